@@ -1,0 +1,369 @@
+"""Benchmark of the Medusa tree-verification step on one GB300 (or N replicas).
+
+One step = tree_attn_paged + tree_accept_greedy + kv_commit over one batch of
+the serving workload (batch 16, 32 q / 8 kv heads, D 128, bf16, prefixes
+uniform in [512, 8192], 64-node trees, bf16 logits over a 32000 vocab), inputs
+resident in HBM.  Between steps (outside the timed events) the block tables and
+sequence lengths are restored and L2 is flushed by writing a 256 MiB buffer.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified tree tokens/s & tree-attn KV GB/s (% of GB300 HBM roofline), 1 GPU"
+UNIT = "tree tokens/s"
+DEFAULT_WORKLOAD = "serve_b16_gqa_bf16"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=1)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("hbm_gbs"), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def algorithmic_bytes(w_host: dict) -> dict:
+    """Bytes the path must move at least once (per step)."""
+    es = {"f32": 4, "f16": 2, "bf16": 2}[w_host["dtype"]]
+    B, T, Hq, Hkv, D = w_host["B"], w_host["T"], w_host["Hq"], w_host["Hkv"], w_host["head_dim"]
+    L = np.asarray(w_host["seq_lens_host"] if "seq_lens_host" in w_host else w_host["seq_lens"], np.int64)
+    prefix_kv = int(L.sum()) * Hkv * D * 2 * es
+    tree_qo = B * T * Hq * D * 2 * es              # q read, out written
+    tree_kv = B * T * Hkv * D * 2 * es             # the tree's own K/V
+    attn = prefix_kv + tree_qo + tree_kv
+    logits = 0
+    if "vocab" in w_host:
+        les = {"f32": 4, "f16": 2, "bf16": 2}[w_host["logits_dtype"]]
+        logits = B * T * w_host["vocab"] * les
+    return dict(prefix_kv=prefix_kv, tree_qo=tree_qo, tree_kv=tree_kv, attn=attn, logits=logits)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import medusa_tree_speculative_attn_gb300 as mt
+    import workloads
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    w = workloads.generate(args.workload, seed=args.seed + 1000 * rank, backend="torch", device=str(dev))
+    spec = w["spec"]
+    B, T, md = w["B"], w["T"], w["max_depth"]
+    stream = torch.cuda.current_stream()
+    rope = mt.Rope(w["rope_base"], w["head_dim"], int(w["seq_lens_host"].max()) + T + 1)
+    desc = mt.make_desc(w["q"], w["k_cache"], w["block_tables"], args.splits, args.kernel)
+    ws = mt.alloc_attn_workspace(desc, dev)
+    aws = mt.alloc_accept_workspace(B, T, dev)
+    out = torch.empty_like(w["q"])
+    am = torch.empty((B, T), dtype=torch.int32, device=dev)
+    alen = torch.empty(B, dtype=torch.int32, device=dev)
+    path = torch.empty((B, md + 1), dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    rel = torch.empty((B, mt.released_width(T, w["page_size"])), dtype=torch.int32, device=dev)
+    bt0, sl0 = w["block_tables"].clone(), w["seq_lens"].clone()
+    has_accept = "logits" in w
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def restore():
+        w["block_tables"].copy_(bt0)
+        w["seq_lens"].copy_(sl0)
+
+    def step(src=None):
+        s = src or w
+        mt.tree_attn_paged(s["q"], w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"],
+                           s["tree_parents"], s["tree_depths"], out, k_new=s["k_new"], v_new=s["v_new"],
+                           rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel)
+        if has_accept:
+            mt.tree_accept_greedy(s["tree_tokens"], s["logits"], s["tree_parents"], alen, path,
+                                  argmax_out=am, next_token=nxt, workspace=aws)
+            mt.kv_commit(path, alen, w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
+                         tree_size=T, status_ws=ws)
+
+    for _ in range(args.warmup):
+        restore()
+        step()
+    torch.cuda.synchronize()
+    st = mt.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    mt.profile_enable(K)
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    accepted = 0
+    for k in range(K):
+        restore()
+        flush.fill_(k & 0xFF)
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    main_ms = mt.profile_read(K)
+    mt.profile_enable(0)
+    if has_accept:
+        accepted = int(alen.sum().item()) + B
+    st = mt.read_status(ws)
+    if st != 0 or (has_accept and mt.read_status(aws) != 0):
+        raise RuntimeError(f"device status {st} after timed steps")
+    ms = float(np.mean(step_ms))
+    t_max = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(t.item())
+
+    # end to end through the public API with host buffers: pinned H2D of the
+    # step's inputs, the three calls, D2H of the step's results
+    e2e = None
+    if not args.no_e2e:
+        keys_in = ["q", "k_new", "v_new", "tree_parents", "tree_depths"]
+        if has_accept:
+            keys_in += ["tree_tokens", "logits"]
+        host = {k: w[k].cpu().pin_memory() for k in keys_in}
+        dsrc = {k: torch.empty_like(w[k]) for k in keys_in}
+        outs = [out, am, alen, path, nxt, rel] if has_accept else [out]
+        houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(host[k].numel() * host[k].element_size() for k in keys_in)
+        d2h = sum(o.numel() * o.element_size() for o in outs)
+        eev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for k in range(K + 2):
+            restore()
+            flush.fill_(k & 0xFF)
+            if k >= 2:
+                eev[k - 2][0].record(stream)
+            for key in keys_in:
+                dsrc[key].copy_(host[key], non_blocking=True)
+            step(dsrc)
+            for o, ho in zip(outs, houts):
+                ho.copy_(o, non_blocking=True)
+            if k >= 2:
+                eev[k - 2][1].record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * B * T / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    ab = algorithmic_bytes(w)
+    peak, peak_src = measured_peaks()
+    main_avg = float(np.mean(main_ms)) if main_ms else None
+    roofline = None
+    if main_avg:
+        achieved = ab["attn"] / (main_avg * 1e-3) / 1e9
+        roofline = {"kernel": "tree attention main kernel", "bound": "hbm", "achieved": achieved,
+                    "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
+                    "traffic": None, "ms_per_launch": main_avg,
+                    "alg_bytes_per_launch": ab["attn"]}
+    res = {
+        "metric": METRIC, "value": world * B * T / (t_max * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "batch": B, "tree_nodes": T, "q_heads": w["Hq"],
+                   "kv_heads": w["Hkv"], "head_dim": w["head_dim"], "page_size": w["page_size"],
+                   "prefix": list(spec.prefix), "logits": (f"{w['logits_dtype']} vocab {w['vocab']}"
+                                                           if has_accept else None),
+                   "kernel": args.kernel, "num_splits": args.splits,
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "kv_gbs": ab["prefix_kv"] / (main_avg * 1e-3) / 1e9 if main_avg else None,
+        "accepted_tokens_per_s": world * accepted / (t_max * 1e-3) if has_accept else None,
+        "alg_bytes": ab, "roofline": roofline, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": K * (5 if has_accept else 3), "wall_s_timed_region": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_s)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return res
+
+
+def oracle_sample_step(w_np: dict, seqs):
+    """The oracle on the given sequences: attention of every (node, head),
+    greedy acceptance and the commit.  Returns tree tokens processed."""
+    import oracle
+    sub = {k: w_np[k] for k in w_np}
+    q_rot, k_rot = oracle.rotate_inputs(w_np)
+    sel = np.array([(b, h, i) for b in seqs for i in range(w_np["T"]) for h in range(w_np["Hq"])],
+                   np.int32)
+    oracle.tree_attn(w_np, sel=sel, q_rot=q_rot, k_rot=k_rot)
+    if "logits" in w_np:
+        idx = np.asarray(seqs)
+        am, alen, path, nxt = oracle.accept_greedy(w_np["tree_tokens"][idx], w_np["logits"][idx],
+                                                   w_np["logits_dtype"], w_np["tree_parents"][idx],
+                                                   w_np["max_depth"])
+    del sub
+    return len(seqs) * w_np["T"]
+
+
+def cpu_baseline(w, budget_s: float):
+    import oracle
+    import workloads
+    w_np = workloads.to_numpy(w)
+    t0 = time.perf_counter()
+    n = oracle_sample_step(w_np, [0])
+    t1 = time.perf_counter() - t0
+    seqs = list(range(1, min(w_np["B"], 1 + max(0, int(budget_s / max(t1, 1e-3)) - 1))))
+    t0 = time.perf_counter()
+    if seqs:
+        n = oracle_sample_step(w_np, seqs)
+        dt = time.perf_counter() - t0
+    else:
+        dt = t1
+        seqs = [0]
+    return {"value": n / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{len(seqs)} of {w_np['B']} sequences of {w_np['name']}: attention of every "
+                      f"(node, q head) in float64 plus greedy acceptance, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    import oracle
+    import workloads
+    if rank != 0:
+        return None
+    w_np = workloads.generate(args.workload, seed=args.seed)
+    spec = w_np["spec"]
+    # one step = one sequence of the workload (a bounded sample)
+    times = []
+    for k in range(args.warmup + args.steps):
+        b = k % w_np["B"]
+        t0 = time.perf_counter()
+        n = oracle_sample_step(w_np, [b])
+        dt = time.perf_counter() - t0
+        if k >= args.warmup:
+            times.append(dt)
+    ms = 1e3 * float(np.mean(times))
+    value = w_np["T"] / (ms * 1e-3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "batch": w_np["B"], "tree_nodes": w_np["T"],
+                   "q_heads": w_np["Hq"], "kv_heads": w_np["Hkv"], "head_dim": w_np["head_dim"],
+                   "step_sample": "one sequence per step (CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": "one sequence of the workload per step: attention of every "
+                                   "(node, q head) in float64 plus greedy acceptance"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

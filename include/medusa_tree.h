@@ -1,0 +1,218 @@
+/*
+ * medusa_tree.h -- C ABI of the Medusa tree-verification library (sm_103a).
+ *
+ * One verify step of Medusa speculative decoding, for every sequence of a
+ * batch, in three calls on one CUDA stream:
+ *
+ *   mt_tree_attn_paged    the T candidate tokens of the sequence's speculation
+ *                         tree attend, in one pass, to the sequence's paged KV
+ *                         cache plus their own tree ancestors (the "tree mask"),
+ *                         with RoPE applied at position prefix_len + depth;
+ *   mt_tree_accept_greedy per-node vocab argmax of the target logits and the
+ *                         longest root path whose tokens match their parent's
+ *                         argmax;
+ *   mt_kv_commit          the accepted nodes' K/V move into the sequence's next
+ *                         cache slots, the sequence length grows and the tree
+ *                         scratch pages past the new length are released.
+ *
+ * What the pages fix, per call:
+ *  - vLLM issue 1171 "[Discussion] Will vLLM consider using Speculative
+ *    Sampling to accelerating LLM decoding?": several new tokens attend to an
+ *    existing paged KV cache (comment by zhaoyang-star); the Medusa tree mask
+ *    is applied inside the cached-KV attention; block tables are updated when a
+ *    candidate is accepted and the other blocks released; the step returns a
+ *    list of tokens (comment by void-main listing the needed changes); with
+ *    several query tokens per sequence the products belong on tensor cores
+ *    (void-main on PagedFlashAttention).
+ *  - TensorRT-LLM issue 1946 "How to use Medusa to support non llama models?",
+ *    answer by rakib-hasan: a position-offset tensor lets RoPE rotate each
+ *    Medusa token at its own position.
+ *  - lmdeploy PR 1231 "[WIP] support Medusa": greedy acceptance at LM-head
+ *    temperature 0 over a 64-choice tree; a tree-mask kernel in the
+ *    Flash-Decoding style (split keys, merge partial softmaxes).
+ *  - mlc-llm issue 2319 "[Feature Request] Medusa support": tree attention and
+ *    the KV cache update are the two hard parts.
+ *
+ * Conventions (all calls):
+ *  - Every tensor is caller-owned device memory, dense, in the layouts given
+ *    below, 16-byte aligned.  The library allocates device memory only in
+ *    mt_rope_create.
+ *  - Calls are asynchronous on `stream` and never synchronise, except
+ *    mt_read_status and mt_rope_create.
+ *  - Errors the host can see (null pointers, unsupported dtype / head_dim /
+ *    tree size, misalignment, a workspace that is too small) return a negative
+ *    mt_status before anything is launched.  Errors only the device can see
+ *    (malformed trees, page ids out of range, block tables shorter than
+ *    prefix + T slots, a bounded wait that gave up) are recorded in a status
+ *    word inside the workspace and read with mt_read_status; the outputs of
+ *    an affected sequence are then unspecified, and nothing outside the
+ *    caller's buffers is touched.  No kernel traps or asserts.
+ *  - Node order: node 0 is the root (parent -1, depth 0): the token chosen by
+ *    the previous step, not yet in the cache.  Every other node i has
+ *    0 <= parent[i] < i and depth[i] = depth[parent[i]] + 1.  T <= 64.
+ *  - Paged cache layout: k_cache and v_cache are [num_pages][Hkv][P][D] in the
+ *    act dtype; logical slot s of sequence b is row s % P of page
+ *    block_tables[b][s / P].  block_tables is int32 [B][max_blocks_per_seq]
+ *    (unused entries may hold -1); seq_lens is int32 [B], the committed prefix
+ *    length L_b.  The table must cover slots 0 .. L_b + T - 1: slots
+ *    L_b .. L_b + T - 1 are the tree's scratch region.
+ */
+#ifndef MEDUSA_TREE_H_
+#define MEDUSA_TREE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MT_OK = 0,
+  MT_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned, workspace too small */
+  MT_ERR_UNSUPPORTED = -2,  /* dtype / head_dim / page size / tree size not supported */
+  MT_ERR_TREE = -3,         /* (device) parents or depths violate the node-order rule */
+  MT_ERR_PAGES = -4,        /* (device) page id out of range or block table too short */
+  MT_ERR_CUDA = -5,         /* a CUDA runtime call failed */
+  MT_ERR_TIMEOUT = -6       /* (device) a bounded pipeline wait gave up */
+} mt_status;
+
+typedef enum { MT_F32 = 0, MT_F16 = 1, MT_BF16 = 2 } mt_dtype;
+
+/* Kernel choice for mt_tree_attn_paged.  AUTO: tensor cores (tcgen05, TMEM,
+ * TMA) for fp16/bf16, the SIMT kernel for fp32.  SIMT: the CUDA-core kernel for
+ * every dtype (a second, independent implementation used by the tests). */
+typedef enum { MT_KERNEL_AUTO = 0, MT_KERNEL_SIMT = 1, MT_KERNEL_TC = 2 } mt_kernel;
+
+typedef struct {
+  int batch;               /* B >= 1 */
+  int tree_size;           /* T, 1..64 */
+  int num_q_heads;         /* Hq, a multiple of Hkv */
+  int num_kv_heads;        /* Hkv */
+  int head_dim;            /* D: 64 or 128 */
+  int page_size;           /* P: 16 */
+  int max_blocks_per_seq;  /* columns of block_tables */
+  int num_pages;           /* pages in the cache pool */
+  int num_splits;          /* 0: balanced schedule over the whole batch (each
+                              persistent CTA takes an equal share of all key
+                              tiles); n > 0: every (sequence, KV head) is split
+                              into n key chunks merged by a log-sum-exp pass */
+  mt_dtype dtype;          /* q, k_new, v_new, caches and out */
+  float sm_scale;          /* softmax scale; 0 means 1/sqrt(D) */
+  int kernel;              /* an mt_kernel value */
+} mt_attn_desc;
+
+/* ---- RoPE table ----------------------------------------------------------
+ * Library-owned fp32 cos/sin table [max_pos][D/2] on the current device, built
+ * on the host in double precision (NeoX / LLaMA half-split form):
+ *   inv_freq_j = pow(base, -(2j)/D), theta = pos * inv_freq_j (IEEE double),
+ *   stored values (float)cos(theta), (float)sin(theta).
+ * The rotation of a head vector x at position pos, for j < D/2, in fp32 with
+ * each product and sum rounded separately (no fused multiply-add):
+ *   x'[j] = x[j]*c - x[j+D/2]*s,   x'[j+D/2] = x[j+D/2]*c + x[j]*s,
+ * then rounded to nearest-even in the act dtype.  Tree token i of sequence b is
+ * rotated at pos = seq_lens[b] + tree_depths[b][i] (the Medusa position offset,
+ * TensorRT-LLM issue 1946).  max_pos must exceed every such position.
+ * mt_rope_create allocates and synchronises the current device; destroy frees. */
+typedef struct mt_rope mt_rope;
+int mt_rope_create(double base, int head_dim, int max_pos, mt_rope** out);
+int mt_rope_destroy(mt_rope* rope);
+
+/* ---- Tree attention -------------------------------------------------------
+ * For each sequence b, tree node i and query head h (KV head h / (Hq/Hkv)):
+ *   out[b][i][h] = sum_j softmax_j(q'.k_j * sm_scale) v_j
+ * over the keys j = prefix slots 0 .. L_b-1 of the paged cache, plus the tree
+ * keys of i's ancestors, i itself included.  q' and the tree keys are rotated
+ * at position L_b + depth[i]; the prefix keys are used as stored.  Before the
+ * attention, node i's rotated key and raw value are written to logical slot
+ * L_b + i (the scratch region), where mt_kv_commit later finds them; slots
+ * below L_b are never written.  Accumulation in fp32, output rounded to nearest
+ * even in the act dtype.
+ *   q      [B][T][Hq][D]    act   (not rotated)
+ *   k_new  [B][T][Hkv][D]   act   (the tree tokens' keys, not rotated)
+ *   v_new  [B][T][Hkv][D]   act
+ *   k_cache, v_cache        act   paged layout above (written: scratch slots)
+ *   block_tables, seq_lens  int32 (read only)
+ *   tree_parents, tree_depths int32 [B][T]
+ *   out    [B][T][Hq][D]    act
+ *   workspace: device memory of mt_tree_attn_workspace_size(desc) bytes,
+ *     zero-filled before its first use; it holds the device status word, the
+ *     ancestor bitmasks, the schedule and the split-KV partial results.  One
+ *     workspace per stream: calls sharing a workspace must not overlap. */
+size_t mt_tree_attn_workspace_size(const mt_attn_desc* desc);
+int mt_tree_attn_paged(const mt_attn_desc* desc, const void* q, const void* k_new,
+                       const void* v_new, void* k_cache, void* v_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens,
+                       const int32_t* tree_parents, const int32_t* tree_depths,
+                       const mt_rope* rope, void* out, void* workspace, size_t ws_bytes,
+                       cudaStream_t stream);
+
+/* ---- Greedy acceptance ----------------------------------------------------
+ * Per sequence b (LM head at temperature 0):
+ *   argmax_out[b][i] = argmax_v target_logits[b][i][v], the lowest index among
+ *                      equal maxima (values compared exactly; +0 equals -0);
+ *   node 0 is accepted; node i > 0 is accepted when its parent is and
+ *     tree_tokens[b][i] == argmax_out[b][parent[i]];
+ *   end = the accepted node of largest depth, the lowest index among equals;
+ *   accept_len[b]  = depth of end (accepted tokens besides the root);
+ *   accept_path[b] = node ids root .. end, then -1, max_depth+1 entries;
+ *   next_token[b]  = argmax_out[b][end], the token the target model adds.
+ *   tree_tokens int32 [B][T]; target_logits [B][T][V] in logits_dtype (no NaN);
+ *   tree_parents int32 [B][T]; every depth must be <= max_depth.
+ *   workspace: mt_tree_accept_workspace_size(B, T) bytes, zero-filled before
+ *   first use (status word and per-sequence arrival counters, which every call
+ *   leaves at zero). */
+size_t mt_tree_accept_workspace_size(int batch, int tree_size);
+int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
+                          mt_dtype logits_dtype, const int32_t* tree_tokens,
+                          const void* target_logits, const int32_t* tree_parents,
+                          int32_t* argmax_out, int32_t* accept_len, int32_t* accept_path,
+                          int32_t* next_token, void* workspace, size_t ws_bytes,
+                          cudaStream_t stream);
+
+/* ---- KV commit --------------------------------------------------------------
+ * For each sequence b, with L = accept_len[b] and len = seq_lens[b]:
+ *   for d = 0..L: every KV head's K and V row at logical slot
+ *     len + accept_path[b][d] is copied to slot len + d (all sources of a
+ *     sequence are read before any destination is written);
+ *   seq_lens[b] = len + L + 1;
+ *   every logical block p with p*P >= len + L + 1 and p*P < len + T (tree
+ *     scratch past the new length) is released: block_tables[b][p] becomes -1
+ *     and its page id is listed, in ascending p, in released_pages[b][*], a row
+ *     of (T + 2P - 2) / P entries padded with -1.
+ *   accept_path int32 [B][max_depth+1], accept_len int32 [B] (as produced by
+ *   mt_tree_accept_greedy); k_cache, v_cache, block_tables, seq_lens are
+ *   updated in place.  desc supplies B, T, Hkv, D, P, max_blocks_per_seq,
+ *   num_pages and dtype.  status_ws: at least 256 bytes of device memory whose
+ *   first int32 is the device status word (the attention workspace serves). */
+int mt_kv_commit(const mt_attn_desc* desc, int max_depth, const int32_t* accept_path,
+                 const int32_t* accept_len, void* k_cache, void* v_cache,
+                 int32_t* block_tables, int32_t* seq_lens, int32_t* released_pages,
+                 void* status_ws, cudaStream_t stream);
+
+/* ---- Status ------------------------------------------------------------------
+ * Waits for `stream`, then reads and clears the device status word at the start
+ * of `workspace` (MT_OK or the first device-side error since the last read). */
+int mt_read_status(void* workspace, cudaStream_t stream, int* device_status);
+const char* mt_status_string(int status);
+
+/* ---- Profiling hook -----------------------------------------------------------
+ * mt_profile_enable(n) creates n pairs of CUDA events (0 disables and frees
+ * them).  While fewer than n pairs are used, each mt_tree_attn_paged call
+ * records one pair on its stream, immediately around its main attention kernel
+ * (the ancestor/scatter preparation and the split-KV combine are outside it).
+ * mt_profile_read waits for the recorded pairs, writes their elapsed times in
+ * milliseconds to ms[0 .. *n_out-1] and starts over.  Not thread-safe: for one
+ * host thread driving the library. */
+int mt_profile_enable(int max_records);
+int mt_profile_read(float* ms, int max_records, int* n_out);
+
+/* Version of this ABI: major * 10000 + minor * 100 + patch. */
+int mt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEDUSA_TREE_H_ */

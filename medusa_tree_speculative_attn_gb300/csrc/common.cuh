@@ -1,0 +1,186 @@
+// Shared device-side definitions of the Medusa tree-verification kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace mt {
+
+constexpr int kTileKeys = 64;   // logical slots per attention key tile
+constexpr int kMaxTree = 64;    // one uint64 ancestor mask per node
+
+// Device status codes (match mt_status in the public header).
+enum : int { kStOk = 0, kStTree = -3, kStPages = -4, kStTimeout = -6 };
+
+// First error wins; later ones are dropped.
+__device__ __forceinline__ void set_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// ---------------------------------------------------------------------------
+// act dtype traits: exact widening to fp32, round-to-nearest-even narrowing.
+// ---------------------------------------------------------------------------
+template <typename T> struct Act;
+template <> struct Act<float> {
+  static __device__ __forceinline__ float to_f(float x) { return x; }
+  static __device__ __forceinline__ float from_f(float x) { return x; }
+};
+template <> struct Act<__half> {
+  static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+  static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+template <> struct Act<__nv_bfloat16> {
+  static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  static __device__ __forceinline__ __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+// RoPE on one (j, j + D/2) pair, each product and difference rounded on its
+// own (no fused multiply-add), so the result is bit-identical to the plain
+// fp32 definition: lo' = lo*c - hi*s, hi' = hi*c + lo*s.
+__device__ __forceinline__ void rope_pair(float lo, float hi, float c, float s, float& out_lo,
+                                          float& out_hi) {
+  out_lo = __fsub_rn(__fmul_rn(lo, c), __fmul_rn(hi, s));
+  out_hi = __fadd_rn(__fmul_rn(hi, c), __fmul_rn(lo, s));
+}
+
+// ---------------------------------------------------------------------------
+// Work schedule shared by the prep, attention and combine kernels.
+//
+// A segment is (sequence b, KV head, row group): the rows_per_group query rows
+// (node i, head-in-group hh) -> row i*g + hh of one KV head, against the
+// sequence's n_b = L_b + T logical key slots, cut into ceil(n_b / 64) tiles.
+// Segments are numbered b-major: s = (b * Hkv + kvh) * nrg + rg, and the tiles
+// of all segments form one global list in that order.  tile_pfx[b] is the
+// number of tiles of one segment of every sequence before b (so sequence b's
+// segments start at tile_pfx[b] * Hkv * nrg).
+//
+// splits == 0 (balanced): CTA c of G takes global tiles [c*W/G, (c+1)*W/G).
+//   The part of one segment that a CTA takes is a piece; a piece that is a
+//   whole segment writes the output directly, any other piece writes a
+//   partial result to slot s + c (unique: CTAs touching a later segment never
+//   have a smaller index).
+// splits == n > 0: segment s is cut into n key chunks of equal tile counts;
+//   chunk k is a piece with partial slot s*n + k (direct output when n == 1);
+//   the U = nseg*n pieces are dealt to CTAs in contiguous runs.
+// ---------------------------------------------------------------------------
+struct Sched {
+  int B, T, Hkv, nrg, G, splits;
+  const int* tile_pfx;  // [B + 1]
+};
+
+struct Piece {
+  int b, kvh, rg, seg;
+  int tile_begin, tile_end;  // tiles of the segment covered by this piece
+  int slot;                  // partial slot, or -1 for a direct write
+};
+
+__device__ __forceinline__ long long sched_total_tiles(const Sched& s) {
+  return (long long)s.tile_pfx[s.B] * s.Hkv * s.nrg;
+}
+
+// Largest b with tile_pfx[b] * HR <= t (the sequence owning global tile t).
+__device__ __forceinline__ int sched_find_seq(const Sched& s, long long t) {
+  long long HR = (long long)s.Hkv * s.nrg;
+  int lo = 0, hi = s.B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((long long)s.tile_pfx[mid] * HR <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// CTA that owns global tile t in balanced mode.
+__device__ __forceinline__ int sched_cta_of(long long t, long long W, int G) {
+  return (int)(((t + 1) * (long long)G - 1) / W);
+}
+
+// Iterator over the pieces of one CTA.
+struct PieceIter {
+  Sched s;
+  int cta;
+  long long cur, end;  // balanced: global tile cursor; split mode: unit cursor
+  long long W;
+
+  __device__ void init(const Sched& sc, int c) {
+    s = sc;
+    cta = c;
+    if (s.splits == 0) {
+      W = sched_total_tiles(s);
+      cur = W * c / s.G;
+      end = W * (c + 1) / s.G;
+    } else {
+      W = (long long)s.B * s.Hkv * s.nrg * s.splits;
+      cur = W * c / s.G;
+      end = W * (c + 1) / s.G;
+    }
+  }
+
+  // Returns false when the CTA has no more work.
+  __device__ bool next(Piece& p) {
+    long long HR = (long long)s.Hkv * s.nrg;
+    while (cur < end) {
+      if (s.splits == 0) {
+        int b = sched_find_seq(s, cur);
+        int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
+        long long local = cur - (long long)s.tile_pfx[b] * HR;
+        int seg_in_b = (int)(local / nt);
+        int j0 = (int)(local % nt);
+        long long seg_begin = cur - j0;
+        long long seg_end = seg_begin + nt;
+        long long stop = end < seg_end ? end : seg_end;
+        p.b = b;
+        p.kvh = seg_in_b / s.nrg;
+        p.rg = seg_in_b % s.nrg;
+        p.seg = (int)((long long)b * HR + seg_in_b);
+        p.tile_begin = j0;
+        p.tile_end = j0 + (int)(stop - cur);
+        p.slot = (j0 == 0 && stop == seg_end) ? -1 : p.seg + cta;
+        cur = stop;
+        return true;
+      } else {
+        long long u = cur++;
+        int k = (int)(u % s.splits);
+        int seg = (int)(u / s.splits);
+        int b = (int)(seg / HR);
+        int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
+        int j0 = (int)((long long)nt * k / s.splits);
+        int j1 = (int)((long long)nt * (k + 1) / s.splits);
+        if (j0 >= j1) continue;
+        int seg_in_b = (int)(seg - (long long)b * HR);
+        p.b = b;
+        p.kvh = seg_in_b / s.nrg;
+        p.rg = seg_in_b % s.nrg;
+        p.seg = seg;
+        p.tile_begin = j0;
+        p.tile_end = j1;
+        p.slot = s.splits == 1 ? -1 : seg * s.splits + k;
+        return true;
+      }
+    }
+    return false;
+  }
+};
+
+// Arguments shared by both attention kernels and the combine kernel.
+struct AttnParams {
+  int B, T, Hq, Hkv, D, P, max_blocks, num_pages, g;
+  int rows;            // T * g query rows per (b, kvh)
+  int rows_per_group;  // RG
+  float scale_log2;    // sm_scale * log2(e)
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int* block_tables;
+  const int* seq_lens;
+  const int* tree_depths;
+  const float2* rope;  // [max_pos][D/2] (cos, sin)
+  int max_pos;
+  void* out;
+  int* status;
+  const unsigned long long* anc;  // [B][T]
+  float* part_o;                  // [slots][RG][D]
+  float2* part_ml;                // [slots][RG] (max in log2 units, sum)
+  Sched sched;
+};
+
+}  // namespace mt

@@ -1,0 +1,63 @@
+// Kernel parameter blocks and launchers (internal to the library).
+#pragma once
+
+#include "common.cuh"
+
+namespace mt {
+
+struct PrepParams {
+  int B, T, Hkv, D, P, max_blocks, num_pages, max_pos;
+  const void* k_new;
+  const void* v_new;
+  void* k_cache;
+  void* v_cache;
+  const int* block_tables;
+  const int* seq_lens;
+  const int* tree_parents;
+  const int* tree_depths;
+  const float2* rope;
+  int* status;
+  unsigned long long* anc;  // [B][T]
+  int* tile_pfx;            // [B + 1]
+};
+
+struct AcceptParams {
+  int B, T, V, max_depth;
+  const int* tokens;
+  const void* logits;
+  const int* parents;
+  int* argmax_out;
+  int* accept_len;
+  int* accept_path;
+  int* next_token;
+  int* status;
+  unsigned int* counters;  // [B], left at zero
+};
+
+struct CommitParams {
+  int B, T, Hkv, D, P, max_blocks, num_pages, max_depth, rel_width, elem_bytes;
+  const int* accept_path;
+  const int* accept_len;
+  void* k_cache;
+  void* v_cache;
+  int* block_tables;
+  int* seq_lens;
+  int* released;
+  int* status;
+};
+
+// Persistent CTAs per SM for each attention kernel.
+constexpr int kSimtRows = 64;
+constexpr int kSimtCtasPerSm = 2;
+constexpr int kTcRows = 256;
+constexpr int kTcCtasPerSm = 1;
+
+cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream);
+cudaError_t launch_attn_simt(const AttnParams& a, int dtype, cudaStream_t stream);
+cudaError_t launch_attn_tc(const AttnParams& a, int dtype, const void* tmap_k, const void* tmap_v,
+                           cudaStream_t stream);
+cudaError_t launch_combine(const AttnParams& a, int dtype, cudaStream_t stream);
+cudaError_t launch_accept(const AcceptParams& a, int dtype, cudaStream_t stream);
+cudaError_t launch_commit(const CommitParams& a, cudaStream_t stream);
+
+}  // namespace mt

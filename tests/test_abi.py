@@ -1,0 +1,117 @@
+"""The C ABI library loads on a machine without a GPU, exports every function
+that include/medusa_tree.h declares, and rejects bad host-side arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "medusa_tree.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from medusa_tree_speculative_attn_gb300 import build
+    build.build()
+    import medusa_tree_speculative_attn_gb300 as mt
+    return mt.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(mt_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("mt_tree_attn_paged", "mt_tree_accept_greedy", "mt_kv_commit",
+              "mt_tree_attn_workspace_size", "mt_tree_accept_workspace_size", "mt_rope_create",
+              "mt_rope_destroy", "mt_read_status", "mt_status_string", "mt_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in medusa_tree.h but not exported"
+
+
+def test_status_strings_and_version(lib):
+    import medusa_tree_speculative_attn_gb300 as mt
+    assert mt.version() == 10000
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert mt.status_string(code) != "unknown status"
+
+
+def _desc(**kw):
+    import medusa_tree_speculative_attn_gb300 as mt
+    base = dict(batch=2, tree_size=8, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
+                max_blocks_per_seq=8, num_pages=32, num_splits=0, dtype=2, sm_scale=0.0, kernel=0)
+    base.update(kw)
+    return mt.AttnDesc(**base)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(tree_size=65), -2), (dict(tree_size=0), -2), (dict(head_dim=96), -2),
+    (dict(page_size=32), -2), (dict(num_q_heads=6, num_kv_heads=4), -1), (dict(batch=0), -1),
+    (dict(dtype=7), -2), (dict(kernel=9), -1), (dict(kernel=2, dtype=0), -2),
+    (dict(num_splits=-1), -1), (dict(sm_scale=float("nan")), -1),
+])
+def test_attn_rejects_bad_descriptors(lib, kw, code):
+    d = _desc(**kw)
+    P = ctypes.c_void_p
+    buf = (ctypes.c_char * 4096)()
+    p = ctypes.cast(buf, P)
+    st = lib.mt_tree_attn_paged(ctypes.byref(d), p, p, p, p, p, p, p, p, p, p, p, p, 4096, None)
+    assert st == code
+    assert lib.mt_tree_attn_workspace_size(ctypes.byref(d)) == 0
+
+
+def test_attn_rejects_null_and_misaligned_pointers(lib):
+    d = _desc()
+    buf = (ctypes.c_char * 4096)()
+    base = ctypes.addressof(buf)
+    al = ctypes.c_void_p((base + 255) // 256 * 256)
+    mis = ctypes.c_void_p(al.value + 4)
+    args = [al] * 12
+    args_null = list(args)
+    args_null[0] = None
+    assert lib.mt_tree_attn_paged(ctypes.byref(d), *args_null, 4096, None) == -1
+    args_mis = list(args)
+    args_mis[0] = mis
+    assert lib.mt_tree_attn_paged(ctypes.byref(d), *args_mis, 4096, None) == -1
+
+
+def test_accept_and_commit_reject_bad_sizes(lib):
+    P = ctypes.c_void_p
+    buf = (ctypes.c_char * 4096)()
+    p = ctypes.cast(buf, P)
+    # tree larger than one 64-bit mask
+    assert lib.mt_tree_accept_greedy(1, 65, 10, 3, 0, p, p, p, p, p, p, p, p, 4096, None) == -2
+    assert lib.mt_tree_accept_greedy(1, 8, 0, 3, 0, p, p, p, p, p, p, p, p, 4096, None) == -1
+    assert lib.mt_tree_accept_greedy(1, 8, 10, 3, 9, p, p, p, p, p, p, p, p, 4096, None) == -2
+    assert lib.mt_tree_accept_greedy(1, 8, 10, 3, 0, None, p, p, p, p, p, p, p, 4096, None) == -1
+    assert lib.mt_tree_accept_workspace_size(0, 8) == 0
+    d = _desc(tree_size=70)
+    assert lib.mt_kv_commit(ctypes.byref(d), 3, p, p, p, p, p, p, p, p, None) == -2
+    d = _desc()
+    assert lib.mt_kv_commit(ctypes.byref(d), 3, None, p, p, p, p, p, p, p, None) == -1
+
+
+def test_rope_create_rejects_bad_arguments(lib):
+    out = ctypes.c_void_p()
+    assert lib.mt_rope_create(10000.0, 96, 100, ctypes.byref(out)) == -1
+    assert lib.mt_rope_create(-1.0, 128, 100, ctypes.byref(out)) == -1
+    assert lib.mt_rope_create(10000.0, 128, 0, ctypes.byref(out)) == -1
+    assert lib.mt_rope_destroy(None) == 0
+
+
+def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
+    import medusa_tree_speculative_attn_gb300 as mt
+    monkeypatch.setattr(mt, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mt, "_lib", None)
+    with pytest.raises(RuntimeError):
+        mt.library()
