@@ -36,8 +36,8 @@ int elem_bytes(mt_dtype dt) { return dt == MT_F32 ? 4 : 2; }
 // Which attention kernel a descriptor runs.
 int select_kernel(const mt_attn_desc* d) {
   if (d->kernel == MT_KERNEL_SIMT) return MT_KERNEL_SIMT;
-  if (d->kernel == MT_KERNEL_TC) return MT_KERNEL_TC;
-  return MT_KERNEL_SIMT;
+  if (d->dtype == MT_F32) return MT_KERNEL_SIMT;
+  return MT_KERNEL_TC;
 }
 
 struct WsLayout {
@@ -221,7 +221,14 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   if (kernel == MT_KERNEL_SIMT) {
     st = cuda_status(launch_attn_simt(ap, d->dtype, stream));
   } else {
-    st = MT_ERR_UNSUPPORTED;  // tensor-core kernel added separately
+    alignas(64) unsigned char tmap_k[128], tmap_v[128];
+    if (make_cache_tmap(tmap_k, k_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
+                        d->head_dim) != cudaSuccess ||
+        make_cache_tmap(tmap_v, v_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
+                        d->head_dim) != cudaSuccess)
+      st = MT_ERR_CUDA;
+    else
+      st = cuda_status(launch_attn_tc(ap, d->dtype, tmap_k, tmap_v, stream));
   }
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n++ + 1], stream);
   if (st != MT_OK) return st;

@@ -54,6 +54,9 @@ constexpr int kTcCtasPerSm = 1;
 
 cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnParams& a, int dtype, cudaStream_t stream);
+// Encodes a TMA descriptor (128 bytes, 64-byte aligned) for a paged cache.
+cudaError_t make_cache_tmap(void* map_out, const void* base, int dtype, int num_pages, int Hkv,
+                            int P, int D);
 cudaError_t launch_attn_tc(const AttnParams& a, int dtype, const void* tmap_k, const void* tmap_v,
                            cudaStream_t stream);
 cudaError_t launch_combine(const AttnParams& a, int dtype, cudaStream_t stream);

@@ -15,7 +15,7 @@ from gpu_helpers import TOL, Step, sample_triples, to_host
 
 pytestmark = pytest.mark.gpu
 
-KERNELS_16 = ["simt"]
+KERNELS_16 = ["simt", "tc"]
 
 
 def _kernels(dtype):
