@@ -36,12 +36,13 @@ int elem_bytes(mt_dtype dt) { return dt == MT_F32 ? 4 : 2; }
 // Which attention kernel a descriptor runs.
 int select_kernel(const mt_attn_desc* d) {
   if (d->kernel == MT_KERNEL_SIMT) return MT_KERNEL_SIMT;
+  if (d->kernel == MT_KERNEL_TC) return MT_KERNEL_TC;
   if (d->dtype == MT_F32) return MT_KERNEL_SIMT;
-  return MT_KERNEL_TC;
+  return tc_supported(d->head_dim, d->num_q_heads / d->num_kv_heads) ? MT_KERNEL_TC : MT_KERNEL_SIMT;
 }
 
 struct WsLayout {
-  size_t anc, pfx, ml, o, total;
+  size_t anc, pfx, qrot, ml, o, total;
   int rows, rows_per_group, nrg, G, nslots;
 };
 
@@ -71,6 +72,9 @@ int layout_for(const mt_attn_desc* d, int kernel, WsLayout* w) {
   off = align_up(off + sizeof(unsigned long long) * (size_t)d->batch * d->tree_size);
   w->pfx = off;
   off = align_up(off + sizeof(int) * (size_t)(d->batch + 1));
+  w->qrot = off;
+  off = align_up(off + (size_t)elem_bytes(d->dtype) * d->batch * d->tree_size * d->num_q_heads *
+                           d->head_dim);
   w->ml = off;
   off = align_up(off + sizeof(float2) * (size_t)nslots * w->rows_per_group);
   w->o = off;
@@ -93,7 +97,9 @@ int check_desc(const mt_attn_desc* d) {
   if (d->num_splits < 0 || d->num_splits > 4096) return MT_ERR_INVALID_ARG;
   if (d->dtype != MT_F32 && d->dtype != MT_F16 && d->dtype != MT_BF16) return MT_ERR_UNSUPPORTED;
   if (d->kernel < MT_KERNEL_AUTO || d->kernel > MT_KERNEL_TC) return MT_ERR_INVALID_ARG;
-  if (d->kernel == MT_KERNEL_TC && d->dtype == MT_F32) return MT_ERR_UNSUPPORTED;
+  if (d->kernel == MT_KERNEL_TC &&
+      (d->dtype == MT_F32 || !tc_supported(d->head_dim, d->num_q_heads / d->num_kv_heads)))
+    return MT_ERR_UNSUPPORTED;
   if (!(d->sm_scale >= 0.f) || std::isinf(d->sm_scale)) return MT_ERR_INVALID_ARG;
   return MT_OK;
 }
@@ -188,9 +194,11 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   char* ws = static_cast<char*>(workspace);
   int* status = reinterpret_cast<int*>(ws);
   PrepParams pp{};
-  pp.B = d->batch; pp.T = d->tree_size; pp.Hkv = d->num_kv_heads; pp.D = d->head_dim;
+  pp.B = d->batch; pp.T = d->tree_size; pp.Hq = d->num_q_heads; pp.Hkv = d->num_kv_heads;
+  pp.D = d->head_dim;
   pp.P = d->page_size; pp.max_blocks = d->max_blocks_per_seq; pp.num_pages = d->num_pages;
   pp.max_pos = rope->max_pos;
+  pp.q = q; pp.q_rot = ws + w.qrot;
   pp.k_new = k_new; pp.v_new = v_new; pp.k_cache = k_cache; pp.v_cache = v_cache;
   pp.block_tables = block_tables; pp.seq_lens = seq_lens;
   pp.tree_parents = tree_parents; pp.tree_depths = tree_depths;
@@ -207,11 +215,11 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   ap.rows = w.rows; ap.rows_per_group = w.rows_per_group;
   const float scale = d->sm_scale > 0.f ? d->sm_scale : (float)(1.0 / std::sqrt((double)d->head_dim));
   ap.scale_log2 = scale * 1.4426950408889634f;
-  ap.q = q; ap.k_cache = k_cache; ap.v_cache = v_cache;
+  ap.q_rot = ws + w.qrot; ap.k_cache = k_cache; ap.v_cache = v_cache;
   ap.block_tables = block_tables; ap.seq_lens = seq_lens; ap.tree_depths = tree_depths;
-  ap.rope = rope->table; ap.max_pos = rope->max_pos; ap.out = out; ap.status = status;
+  ap.out = out; ap.status = status;
   ap.anc = pp.anc;
-  ap.part_o = reinterpret_cast<float*>(ws + w.o);
+  ap.part_o = reinterpret_cast<float4*>(ws + w.o);
   ap.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   ap.sched.B = d->batch; ap.sched.T = d->tree_size; ap.sched.Hkv = d->num_kv_heads;
   ap.sched.nrg = w.nrg; ap.sched.G = w.G; ap.sched.splits = d->num_splits;
@@ -221,14 +229,16 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   if (kernel == MT_KERNEL_SIMT) {
     st = cuda_status(launch_attn_simt(ap, d->dtype, stream));
   } else {
-    alignas(64) unsigned char tmap_k[128], tmap_v[128];
+    alignas(64) unsigned char tmap_k[128], tmap_v[128], tmap_q[128];
     if (make_cache_tmap(tmap_k, k_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
                         d->head_dim) != cudaSuccess ||
         make_cache_tmap(tmap_v, v_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
-                        d->head_dim) != cudaSuccess)
+                        d->head_dim) != cudaSuccess ||
+        make_q_tmap(tmap_q, ws + w.qrot, d->dtype, d->batch * d->tree_size, d->num_q_heads, ap.g,
+                    d->head_dim) != cudaSuccess)
       st = MT_ERR_CUDA;
     else
-      st = cuda_status(launch_attn_tc(ap, d->dtype, tmap_k, tmap_v, stream));
+      st = cuda_status(launch_attn_tc(ap, d->dtype, tmap_k, tmap_v, tmap_q, stream));
   }
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n++ + 1], stream);
   if (st != MT_OK) return st;

@@ -53,7 +53,6 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
   constexpr int LD = D + 1;
   constexpr int PLD = kTileKeys + 1;
   constexpr int NC = D / 16;
-  constexpr int H = D / 2;
   extern __shared__ float smem[];
   float* Qs = smem;               // [R][LD]
   float* KV = Qs + R * LD;        // [64][LD]
@@ -61,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
   __shared__ unsigned long long s_anc[R];
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const T* __restrict__ q = static_cast<const T*>(a.q);
+  const T* __restrict__ q = static_cast<const T*>(a.q_rot);
   const T* __restrict__ kc = static_cast<const T*>(a.k_cache);
   const T* __restrict__ vc = static_cast<const T*>(a.v_cache);
 
@@ -77,27 +76,16 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
       const int row = row0 + r;
       s_anc[r] = row < a.rows ? a.anc[(size_t)b * a.T + row / a.g] : ~0ull;
     }
-    // query rows, rotated at L_b + depth and rounded to the act dtype
-    for (int e = tid; e < R * H; e += blockDim.x) {
-      const int r = e / H, j = e % H;
+    // query rows (rotated at L_b + depth and rounded by the prep kernel)
+    for (int e = tid; e < R * D; e += blockDim.x) {
+      const int r = e / D, d = e % D;
       const int row = row0 + r;
-      float lo = 0.f, hi = 0.f;
+      float v = 0.f;
       if (row < a.rows) {
         const int node = row / a.g, h = kvh * a.g + row % a.g;
-        const T* qr = q + (((size_t)b * a.T + node) * a.Hq + h) * D;
-        const int pos = L + a.tree_depths[(size_t)b * a.T + node];
-        if (pos >= 0 && pos < a.max_pos) {
-          const float2 cs = a.rope[(size_t)pos * H + j];
-          float olo, ohi;
-          rope_pair(Act<T>::to_f(qr[j]), Act<T>::to_f(qr[j + H]), cs.x, cs.y, olo, ohi);
-          lo = Act<T>::to_f(Act<T>::from_f(olo));
-          hi = Act<T>::to_f(Act<T>::from_f(ohi));
-        } else {
-          set_status(a.status, kStTree);
-        }
+        v = Act<T>::to_f(q[(((size_t)b * a.T + node) * a.Hq + h) * D + d]);
       }
-      Qs[r * LD + j] = lo;
-      Qs[r * LD + j + H] = hi;
+      Qs[r * LD + d] = v;
     }
     float m[4], l[4], o[4][NC];
 #pragma unroll
@@ -192,9 +180,12 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
 #pragma unroll
         for (int c = 0; c < NC; ++c) dst[tx + 16 * c] = Act<T>::from_f(o[i][c] * inv);
       } else {
-        float* dst = a.part_o + ((size_t)pc.slot * R + r) * D;
+        float* dst = reinterpret_cast<float*>(a.part_o);
 #pragma unroll
-        for (int c = 0; c < NC; ++c) dst[tx + 16 * c] = o[i][c];
+        for (int c = 0; c < NC; ++c) {
+          const int col = tx + 16 * c;
+          dst[(((size_t)pc.slot * (D / 4) + col / 4) * R + r) * 4 + col % 4] = o[i][c];
+        }
         if (tx == 0) a.part_ml[(size_t)pc.slot * R + r] = make_float2(m[i], l[i]);
       }
     }

@@ -12,17 +12,16 @@ namespace {
 
 constexpr int kWarps = 8;
 
-template <int N> struct VecF;
-template <> struct VecF<4> { using type = float4; };
-template <> struct VecF<2> { using type = float2; };
-
+// Block: 32 rows (one per lane) x 8 warps, warp w handles the 4-column groups
+// w, w + 8, ...; partial reads are coalesced along rows.
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
-  constexpr int PER = D / 32;
+  constexpr int C4 = D / 4;                 // 4-column groups per row
+  constexpr int PER = C4 / kWarps;          // groups per thread
   const Sched& s = a.sched;
   const int seg = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.y * kWarps + warp;
+  const int r = blockIdx.y * 32 + lane;
   const int RG = a.rows_per_group;
   const int HR = s.Hkv * s.nrg;
   const int b = seg / HR, seg_in_b = seg % HR;
@@ -59,34 +58,44 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
   float M = -INFINITY;
   for (int k = 0; k < count; ++k)
     if (piece_exists(k)) M = fmaxf(M, a.part_ml[(size_t)(slot0 + k) * RG + r].x);
-  float acc[PER];
+  float4 acc[PER];
 #pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   float lsum = 0.f;
   if (M != -INFINITY) {
     for (int k = 0; k < count; ++k) {
       if (!piece_exists(k)) continue;
-      const float2 ml = a.part_ml[(size_t)(slot0 + k) * RG + r];
+      const size_t slot = (size_t)(slot0 + k);
+      const float2 ml = a.part_ml[slot * RG + r];
       const float w = exp2f(ml.x - M);
       lsum += w * ml.y;
-      const float* src = a.part_o + ((size_t)(slot0 + k) * RG + r) * D + lane * PER;
-      typename VecF<PER>::type v = *reinterpret_cast<const typename VecF<PER>::type*>(src);
-      const float* vf = reinterpret_cast<const float*>(&v);
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, vf[e], acc[e]);
+      for (int e = 0; e < PER; ++e) {
+        const float4 v = a.part_o[(slot * C4 + warp + kWarps * e) * RG + r];
+        acc[e].x = fmaf(w, v.x, acc[e].x);
+        acc[e].y = fmaf(w, v.y, acc[e].y);
+        acc[e].z = fmaf(w, v.z, acc[e].z);
+        acc[e].w = fmaf(w, v.w, acc[e].w);
+      }
     }
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const int node = row / a.g, h = kvh * a.g + row % a.g;
-  T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D + lane * PER;
+  T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) dst[e] = Act<T>::from_f(acc[e] * inv);
+  for (int e = 0; e < PER; ++e) {
+    const int c = 4 * (warp + kWarps * e);
+    dst[c] = Act<T>::from_f(acc[e].x * inv);
+    dst[c + 1] = Act<T>::from_f(acc[e].y * inv);
+    dst[c + 2] = Act<T>::from_f(acc[e].z * inv);
+    dst[c + 3] = Act<T>::from_f(acc[e].w * inv);
+  }
 }
 
 template <typename T, int D>
 cudaError_t launch_t(const AttnParams& a, cudaStream_t stream) {
   const int nseg = a.B * a.Hkv * a.sched.nrg;
-  dim3 grid(nseg, (a.rows_per_group + kWarps - 1) / kWarps);
+  dim3 grid(nseg, (a.rows_per_group + 31) / 32);
   combine_kernel<T, D><<<grid, kWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }

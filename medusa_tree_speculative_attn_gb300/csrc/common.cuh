@@ -167,18 +167,16 @@ struct AttnParams {
   int rows;            // T * g query rows per (b, kvh)
   int rows_per_group;  // RG
   float scale_log2;    // sm_scale * log2(e)
-  const void* q;
+  const void* q_rot;   // [B][T][Hq][D] act, rotated and rounded (written by prep)
   const void* k_cache;
   const void* v_cache;
   const int* block_tables;
   const int* seq_lens;
   const int* tree_depths;
-  const float2* rope;  // [max_pos][D/2] (cos, sin)
-  int max_pos;
   void* out;
   int* status;
   const unsigned long long* anc;  // [B][T]
-  float* part_o;                  // [slots][RG][D]
+  float4* part_o;                 // [slots][D/4][RG]: unnormalised O, 4 columns per entry
   float2* part_ml;                // [slots][RG] (max in log2 units, sum)
   Sched sched;
 };

@@ -6,7 +6,9 @@
 namespace mt {
 
 struct PrepParams {
-  int B, T, Hkv, D, P, max_blocks, num_pages, max_pos;
+  int B, T, Hq, Hkv, D, P, max_blocks, num_pages, max_pos;
+  const void* q;
+  void* q_rot;  // [B][T][Hq][D] act
   const void* k_new;
   const void* v_new;
   void* k_cache;
@@ -54,11 +56,15 @@ constexpr int kTcCtasPerSm = 1;
 
 cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_attn_simt(const AttnParams& a, int dtype, cudaStream_t stream);
-// Encodes a TMA descriptor (128 bytes, 64-byte aligned) for a paged cache.
+// Encode TMA descriptors (128 bytes, 64-byte aligned): a paged cache, and the
+// rotated queries [B*T][Hq][D] in boxes of 128 rows (128/g nodes x g heads).
 cudaError_t make_cache_tmap(void* map_out, const void* base, int dtype, int num_pages, int Hkv,
                             int P, int D);
+cudaError_t make_q_tmap(void* map_out, const void* base, int dtype, int BT, int Hq, int g, int D);
+// Whether the tensor-core kernel supports a configuration.
+bool tc_supported(int D, int g);
 cudaError_t launch_attn_tc(const AttnParams& a, int dtype, const void* tmap_k, const void* tmap_v,
-                           cudaStream_t stream);
+                           const void* tmap_q, cudaStream_t stream);
 cudaError_t launch_combine(const AttnParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_accept(const AcceptParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& a, cudaStream_t stream);

@@ -1,13 +1,15 @@
 // Tree preparation: validates every sequence's tree, builds the per-node
-// ancestor bitmasks and the tile schedule, and writes the tree tokens' rotated
-// keys and raw values into their scratch slots of the paged cache.
+// ancestor bitmasks and the tile schedule, rotates the tree tokens' queries
+// into the workspace, and writes their rotated keys and raw values into their
+// scratch slots of the paged cache.
 //
 // The tree mask (vLLM issue 1171, void-main: the Medusa tree mask inside the
 // cached-KV attention) is carried as one 64-bit word per node,
 //   anc[i] = anc[parent[i]] | (1 << i),   anc[0] = 1,
 // so node i sees tree key t exactly when bit t of anc[i] is set.  Keys are
 // rotated at position L_b + depth[i] (TensorRT-LLM issue 1946, position
-// offsets for Medusa tokens) and land at logical slot L_b + i.
+// offsets for Medusa tokens); keys land at logical slot L_b + i, queries in a
+// [B][T][Hq][D] workspace array read by the attention kernels.
 #include "kernels.cuh"
 
 namespace mt {
@@ -85,53 +87,63 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
     if (tid == 0) a.tile_pfx[a.B] = total;
     return;
   }
-  // ---- scatter: one warp per (b, node, kv head) row ----
+  // ---- one warp per row: B*T*Hq query rows, then B*T*Hkv key/value rows ----
   const int warp = tid >> 5, lane = tid & 31;
-  const long long row = (long long)blockIdx.x * (kPrepThreads / 32) + warp;
-  const long long nrows = (long long)a.B * a.T * a.Hkv;
-  if (row >= nrows) return;
-  const int kvh = (int)(row % a.Hkv);
-  const int i = (int)((row / a.Hkv) % a.T);
-  const int b = (int)(row / ((long long)a.Hkv * a.T));
+  long long row = (long long)blockIdx.x * (kPrepThreads / 32) + warp;
+  const long long nq = (long long)a.B * a.T * a.Hq;
+  const long long nk = (long long)a.B * a.T * a.Hkv;
+  if (row >= nq + nk) return;
+  const bool is_q = row < nq;
+  if (!is_q) row -= nq;
+  const int H = is_q ? a.Hq : a.Hkv;
+  const int i = (int)((row / H) % a.T);
+  const int b = (int)(row / ((long long)H * a.T));
   const int L = a.seq_lens[b];
   const int depth = a.tree_depths[(size_t)b * a.T + i];
-  const long long slot = (long long)L + i;
   const long long pos = (long long)L + depth;
-  if (L < 0 || slot / a.P >= a.max_blocks) {
-    if (lane == 0) set_status(a.status, kStPages);
-    return;
-  }
-  if (depth < 0 || pos >= a.max_pos) {
-    if (lane == 0) set_status(a.status, kStTree);
-    return;
-  }
-  const int page = a.block_tables[(size_t)b * a.max_blocks + slot / a.P];
-  if (page < 0 || page >= a.num_pages) {
-    if (lane == 0) set_status(a.status, kStPages);
+  if (L < 0 || depth < 0 || pos >= a.max_pos) {
+    if (lane == 0) set_status(a.status, L < 0 ? kStPages : kStTree);
     return;
   }
   const int half = a.D / 2;
-  const T* kn = static_cast<const T*>(a.k_new) + (size_t)row * a.D;
-  const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
-  const size_t dst = (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * a.D;
-  T* kc = static_cast<T*>(a.k_cache) + dst;
-  T* vc = static_cast<T*>(a.v_cache) + dst;
   const float2* cs = a.rope + (size_t)pos * half;
-  for (int j = lane; j < half; j += 32) {
-    float lo = Act<T>::to_f(kn[j]), hi = Act<T>::to_f(kn[j + half]);
-    float2 c = cs[j];
-    float olo, ohi;
-    rope_pair(lo, hi, c.x, c.y, olo, ohi);
-    kc[j] = Act<T>::from_f(olo);
-    kc[j + half] = Act<T>::from_f(ohi);
+  const T* src;
+  T* dst;
+  if (is_q) {
+    src = static_cast<const T*>(a.q) + (size_t)row * a.D;
+    dst = static_cast<T*>(a.q_rot) + (size_t)row * a.D;
+  } else {
+    const int kvh = (int)(row % a.Hkv);
+    const long long slot = (long long)L + i;
+    if (slot / a.P >= a.max_blocks) {
+      if (lane == 0) set_status(a.status, kStPages);
+      return;
+    }
+    const int page = a.block_tables[(size_t)b * a.max_blocks + slot / a.P];
+    if (page < 0 || page >= a.num_pages) {
+      if (lane == 0) set_status(a.status, kStPages);
+      return;
+    }
+    const size_t off = (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * a.D;
+    src = static_cast<const T*>(a.k_new) + (size_t)row * a.D;
+    dst = static_cast<T*>(a.k_cache) + off;
+    const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
+    T* vc = static_cast<T*>(a.v_cache) + off;
+    for (int j = lane; j < a.D; j += 32) vc[j] = vn[j];
   }
-  for (int j = lane; j < a.D; j += 32) vc[j] = vn[j];
+  for (int j = lane; j < half; j += 32) {
+    const float2 c = cs[j];
+    float olo, ohi;
+    rope_pair(Act<T>::to_f(src[j]), Act<T>::to_f(src[j + half]), c.x, c.y, olo, ohi);
+    dst[j] = Act<T>::from_f(olo);
+    dst[j + half] = Act<T>::from_f(ohi);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream) {
-  long long nrows = (long long)a.B * a.T * a.Hkv;
+  long long nrows = (long long)a.B * a.T * ((long long)a.Hq + a.Hkv);
   long long blocks = (nrows + kPrepThreads / 32 - 1) / (kPrepThreads / 32) + 1;
   size_t smem = sizeof(int) * (size_t)(a.B + 1);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
