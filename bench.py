@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
     return ap.parse_args()
 
 
@@ -181,8 +182,59 @@ def run_ours(args, rank, world, local_rank):
         raise RuntimeError(f"device status {st} after warm-up")
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    # (1) kernel-level: per-call events and the main attention kernel's own
+    # duration (library profiling hook), kernels launched one by one
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    evb = [(mk(), mk(), mk(), mk()) for _ in range(K)]
     mt.profile_enable(K)
+    for k in range(K):
+        restore()
+        flush.fill_(k & 0xFF)
+        e0, e1, e2, e3 = evb[k]
+        e0.record(stream)
+        mt.tree_attn_paged(w["q"], w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"],
+                           w["tree_parents"], w["tree_depths"], out, k_new=w["k_new"], v_new=w["v_new"],
+                           rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel)
+        e1.record(stream)
+        if has_accept:
+            mt.tree_accept_greedy(w["tree_tokens"], w["logits"], w["tree_parents"], alen, path,
+                                  argmax_out=am, next_token=nxt, workspace=aws)
+            e2.record(stream)
+            mt.kv_commit(path, alen, w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
+                         tree_size=T, status_ws=ws)
+        else:
+            e2.record(stream)
+        e3.record(stream)
+    torch.cuda.synchronize()
+    main_ms = mt.profile_read(K)
+    mt.profile_enable(0)
+    breakdown = {"tree_attn_paged_ms": float(np.mean([a.elapsed_time(b) for a, b, _, _ in evb])),
+                 "attention_main_kernel_ms": float(np.mean(main_ms)) if main_ms else None,
+                 "tree_accept_greedy_ms": float(np.mean([b.elapsed_time(c) for _, b, c, _ in evb])),
+                 "kv_commit_ms": float(np.mean([c.elapsed_time(d) for _, _, c, d in evb]))}
+
+    # (2) the timed steps: the whole step replayed as one CUDA graph (or
+    # launched kernel by kernel with --no-graph)
+    graph = None
+    if not args.no_graph:
+        restore()
+        gs = torch.cuda.Stream()
+        gs.wait_stream(stream)
+        with torch.cuda.stream(gs):
+            step()                       # warm the capture stream
+            gs.synchronize()
+            restore()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gs):
+                step()
+        stream.wait_stream(gs)
+        torch.cuda.synchronize()
+    run_step = graph.replay if graph is not None else step
+    for _ in range(2):
+        restore()
+        run_step()
+    torch.cuda.synchronize()
+    ev = [(mk(), mk()) for _ in range(K)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -195,7 +247,7 @@ def run_ours(args, rank, world, local_rank):
         restore()
         flush.fill_(k & 0xFF)
         ev[k][0].record(stream)
-        step()
+        run_step()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t_wall
@@ -203,8 +255,6 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     clocks = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    main_ms = mt.profile_read(K)
-    mt.profile_enable(0)
     if has_accept:
         accepted = int(alen.sum().item()) + B
     st = mt.read_status(ws)
@@ -271,10 +321,11 @@ def run_ours(args, rank, world, local_rank):
                    "prefix": list(spec.prefix), "logits": (f"{w['logits_dtype']} vocab {w['vocab']}"
                                                            if has_accept else None),
                    "kernel": args.kernel, "num_splits": args.splits,
+                   "launch": "one CUDA graph per step" if graph is not None else "kernel by kernel",
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "kv_gbs": ab["prefix_kv"] / (main_avg * 1e-3) / 1e9 if main_avg else None,
         "accepted_tokens_per_s": world * accepted / (t_max * 1e-3) if has_accept else None,
-        "alg_bytes": ab, "roofline": roofline, "e2e": e2e, "clocks": clocks,
+        "alg_bytes": ab, "roofline": roofline, "breakdown": breakdown, "e2e": e2e, "clocks": clocks,
         "gpu_launches": K * (5 if has_accept else 3), "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -2,7 +2,9 @@
 // segment (the Flash-Decoding style split that lmdeploy PR 1231 "[WIP] support
 // Medusa" plans for its tree-mask kernel).  For piece k with running maximum
 // m_k (base-2 units), sum l_k and unnormalised output O_k:
-//   M = max_k m_k,  w_k = 2^(m_k - M),  out = sum_k w_k O_k / sum_k w_k l_k.
+//   M = max_k m_k,  w_k = 2^(m_k - M),  out = sum_k w_k O_k / sum_k w_k l_k,
+// evaluated in one pass with a running maximum (pieces that saw no key of a
+// row, m_k = -inf, are skipped).
 // Segments covered by a single piece were written directly and are skipped.
 #include "kernels.cuh"
 
@@ -11,25 +13,29 @@ namespace mt {
 namespace {
 
 constexpr int kWarps = 8;
+constexpr int kMaxListed = 1024;  // pieces listed per pass
 
-// Block: 32 rows (one per lane) x 8 warps, warp w handles the 4-column groups
-// w, w + 8, ...; partial reads are coalesced along rows.
+// Block: one segment, 32 rows.  The piece list is built once per block; each
+// thread then merges one row (lane) for the 4-column groups warp, warp + 8, ...
+// (partial reads coalesced along rows), the block stages the merged rows in
+// shared memory and writes them out in 16-byte chunks along each row.
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
   constexpr int C4 = D / 4;                 // 4-column groups per row
   constexpr int PER = C4 / kWarps;          // groups per thread
+  constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte output chunks per row
+  __shared__ int s_slot[kMaxListed];
+  __shared__ int s_count, s_single;
+  __shared__ __align__(16) T s_out[32][D + 16 / (int)sizeof(T)];
   const Sched& s = a.sched;
   const int seg = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.y * 32 + lane;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int RG = a.rows_per_group;
   const int HR = s.Hkv * s.nrg;
   const int b = seg / HR, seg_in_b = seg % HR;
   const int kvh = seg_in_b / s.nrg, rg = seg_in_b % s.nrg;
-  const int row = rg * RG + r;
-  if (r >= RG || row >= a.rows) return;
   const int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
-  if (nt == 0) return;
+  if (nt == 0) return;  // invalid sequence (block-uniform)
 
   // the slots holding this segment's pieces
   int slot0, count;
@@ -38,7 +44,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
     W = sched_total_tiles(s);
     t0 = (long long)s.tile_pfx[b] * HR + (long long)seg_in_b * nt;
     const int c0 = sched_cta_of(t0, W, s.G), c1 = sched_cta_of(t0 + nt - 1, W, s.G);
-    if (c0 == c1) return;
+    if (c0 == c1) return;  // written directly by its only CTA
     slot0 = seg + c0;
     count = c1 - c0 + 1;
   } else {
@@ -46,49 +52,71 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
     slot0 = seg * s.splits;
     count = s.splits;
   }
-  auto piece_exists = [&](int k) -> bool {
-    if (s.splits == 0) {
-      const int c = slot0 - seg + k;
-      const long long cb = W * c / s.G, ce = W * (c + 1) / s.G;
-      return (cb > t0 ? cb : t0) < (ce < t0 + nt ? ce : t0 + nt);
-    }
-    return (long long)nt * k / s.splits < (long long)nt * (k + 1) / s.splits;
-  };
-
-  float M = -INFINITY;
-  for (int k = 0; k < count; ++k)
-    if (piece_exists(k)) M = fmaxf(M, a.part_ml[(size_t)(slot0 + k) * RG + r].x);
+  const int row0 = blockIdx.y * 32;
+  float M = -INFINITY, lsum = 0.f;
   float4 acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-  if (M != -INFINITY) {
-    for (int k = 0; k < count; ++k) {
-      if (!piece_exists(k)) continue;
-      const size_t slot = (size_t)(slot0 + k);
-      const float2 ml = a.part_ml[slot * RG + r];
-      const float w = exp2f(ml.x - M);
-      lsum += w * ml.y;
+  const int r = row0 + lane;
+  const bool row_ok = r < RG && rg * RG + r < a.rows;
+  for (int k0 = 0; k0 < count; k0 += kMaxListed) {
+    // list the pieces [k0, k0 + kMaxListed) that exist
+    if (tid == 0) s_count = 0;
+    __syncthreads();
+    for (int k = k0 + tid; k < count && k < k0 + kMaxListed; k += blockDim.x) {
+      bool exists;
+      if (s.splits == 0) {
+        const int c = slot0 - seg + k;
+        const long long cb = W * c / s.G, ce = W * (c + 1) / s.G;
+        exists = (cb > t0 ? cb : t0) < (ce < t0 + nt ? ce : t0 + nt);
+      } else {
+        exists = (long long)nt * k / s.splits < (long long)nt * (k + 1) / s.splits;
+      }
+      s_slot[k - k0] = exists ? slot0 + k : -1;
+    }
+    __syncthreads();
+    const int n = min(kMaxListed, count - k0);
+    if (row_ok) {
+      for (int k = 0; k < n; ++k) {
+        const int slot = s_slot[k];
+        if (slot < 0) continue;
+        const float2 ml = a.part_ml[(size_t)slot * RG + r];
+        if (ml.x == -INFINITY) continue;  // the piece saw no key of this row
+        const float m_new = fmaxf(M, ml.x);
+        const float c_old = exp2f(M - m_new), c_new = exp2f(ml.x - m_new);
+        lsum = lsum * c_old + ml.y * c_new;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const float4 v = a.part_o[(slot * C4 + warp + kWarps * e) * RG + r];
-        acc[e].x = fmaf(w, v.x, acc[e].x);
-        acc[e].y = fmaf(w, v.y, acc[e].y);
-        acc[e].z = fmaf(w, v.z, acc[e].z);
-        acc[e].w = fmaf(w, v.w, acc[e].w);
+        for (int e = 0; e < PER; ++e) {
+          const float4 v = a.part_o[((size_t)slot * C4 + warp + kWarps * e) * RG + r];
+          acc[e].x = acc[e].x * c_old + v.x * c_new;
+          acc[e].y = acc[e].y * c_old + v.y * c_new;
+          acc[e].z = acc[e].z * c_old + v.z * c_new;
+          acc[e].w = acc[e].w * c_old + v.w * c_new;
+        }
+        M = m_new;
       }
     }
+    __syncthreads();
   }
   const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  const int node = row / a.g, h = kvh * a.g + row % a.g;
-  T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
     const int c = 4 * (warp + kWarps * e);
-    dst[c] = Act<T>::from_f(acc[e].x * inv);
-    dst[c + 1] = Act<T>::from_f(acc[e].y * inv);
-    dst[c + 2] = Act<T>::from_f(acc[e].z * inv);
-    dst[c + 3] = Act<T>::from_f(acc[e].w * inv);
+    s_out[lane][c] = Act<T>::from_f(acc[e].x * inv);
+    s_out[lane][c + 1] = Act<T>::from_f(acc[e].y * inv);
+    s_out[lane][c + 2] = Act<T>::from_f(acc[e].z * inv);
+    s_out[lane][c + 3] = Act<T>::from_f(acc[e].w * inv);
+  }
+  __syncthreads();
+  // 32 rows x CH chunks, consecutive threads along a row
+  for (int idx = tid; idx < 32 * CH; idx += blockDim.x) {
+    const int lr = idx / CH, ch = idx % CH;
+    const int rr = row0 + lr;
+    const int row = rg * RG + rr;
+    if (rr >= RG || row >= a.rows) continue;
+    const int node = row / a.g, h = kvh * a.g + row % a.g;
+    T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
+    reinterpret_cast<uint4*>(dst)[ch] = *reinterpret_cast<const uint4*>(&s_out[lr][ch * (16 / sizeof(T))]);
   }
 }
 

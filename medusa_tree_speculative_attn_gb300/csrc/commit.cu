@@ -2,8 +2,8 @@
 // 1171, void-main: "update block tables when you accept one candidate and
 // release other blocks"; mlc-llm issue 2319: the KV cache update part).
 //
-// One CTA per sequence.  For each KV head the CTA first reads the K and V rows
-// of every path node (logical slot len + path[d]) into shared memory, then
+// One CTA per sequence.  The CTA first reads the K and V rows of every path
+// node (logical slot len + path[d]) of every KV head into shared memory, then
 // writes them to slots len + d, so a destination that is also a later source
 // (e.g. path [0, 2, 3]: slot len+2 is both) is read before it is overwritten.
 // Afterwards seq_lens[b] grows by accept_len + 1 and every logical block that
@@ -26,23 +26,27 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitParams a) {
   const int* path = a.accept_path + (size_t)b * (a.max_depth + 1);
   const int* bt = a.block_tables + (size_t)b * a.max_blocks;
   const int n = L + 1;
-  if (tid == 0) {
-    int ok = L >= 0 && L <= a.max_depth && L < a.T && len >= 0 &&
-             (long long)len + a.T <= (long long)a.max_blocks * a.P;
-    for (int d = 0; ok && d < n; ++d) {
-      const int node = path[d];
-      if (node < 0 || node >= a.T || (d > 0 && node <= path[d - 1])) ok = 0;
-    }
-    for (int d = 0; ok && d < n; ++d) {
-      const int ss = len + path[d], ds = len + d;
+  if (tid == 0)
+    s_ok = L >= 0 && L <= a.max_depth && L < a.T && len >= 0 &&
+           (long long)len + a.T <= (long long)a.max_blocks * a.P;
+  __syncthreads();
+  if (tid < n && s_ok) {
+    // one thread per path entry: a root path in increasing node order whose
+    // source and destination slots map to pages of the pool
+    const int d = tid;
+    const int node = path[d];
+    bool ok = node >= 0 && node < a.T && (d == 0 || node > path[d - 1]);
+    if (ok) {
+      const int ss = len + node, ds = len + d;
       const int sp = bt[ss / a.P], dp = bt[ds / a.P];
-      if (sp < 0 || sp >= a.num_pages || dp < 0 || dp >= a.num_pages) { ok = 0; break; }
+      ok = sp >= 0 && sp < a.num_pages && dp >= 0 && dp < a.num_pages;
       s_src[d] = sp * a.P + ss % a.P;  // page-row index (per head stride added below)
       s_dst[d] = dp * a.P + ds % a.P;
     }
-    if (!ok) set_status(a.status, kStPages);
-    s_ok = ok;
+    if (!ok) s_ok = 0;
   }
+  __syncthreads();
+  if (tid == 0 && !s_ok) set_status(a.status, kStPages);
   __syncthreads();
   if (!s_ok) return;
   const int row_bytes = a.D * a.elem_bytes;
@@ -51,10 +55,16 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitParams a) {
   const size_t page_stride = (size_t)a.Hkv * head_stride;   // bytes per page
   char* kc = static_cast<char*>(a.k_cache);
   char* vc = static_cast<char*>(a.v_cache);
-  for (int kvh = 0; kvh < a.Hkv; ++kvh) {
-    const int total = n * 2 * rv;
+  // as many KV heads per pass as the staging buffer holds (all of them at the
+  // usual sizes): every source row of the pass is read before any is written
+  const int per_head = n * 2 * rv;
+  const int heads_per_pass = max(1, min(a.Hkv, a.stage_vecs / per_head));
+  for (int h0 = 0; h0 < a.Hkv; h0 += heads_per_pass) {
+    const int nh = min(heads_per_pass, a.Hkv - h0);
+    const int total = nh * per_head;
     for (int e = tid; e < total; e += blockDim.x) {
-      const int d = e / (2 * rv), which = (e / rv) % 2, v = e % rv;
+      const int kvh = h0 + e / per_head, r = e % per_head;
+      const int d = r / (2 * rv), which = (r / rv) % 2, v = r % rv;
       const int pr = s_src[d];
       const size_t off = (size_t)(pr / a.P) * page_stride + kvh * head_stride +
                          (size_t)(pr % a.P) * row_bytes + (size_t)v * 16;
@@ -62,7 +72,8 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitParams a) {
     }
     __syncthreads();
     for (int e = tid; e < total; e += blockDim.x) {
-      const int d = e / (2 * rv), which = (e / rv) % 2, v = e % rv;
+      const int kvh = h0 + e / per_head, r = e % per_head;
+      const int d = r / (2 * rv), which = (r / rv) % 2, v = r % rv;
       const int pr = s_dst[d];
       const size_t off = (size_t)(pr / a.P) * page_stride + kvh * head_stride +
                          (size_t)(pr % a.P) * row_bytes + (size_t)v * 16;
@@ -90,13 +101,18 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitParams a) {
 
 cudaError_t launch_commit(const CommitParams& a, cudaStream_t stream) {
   const int n_max = (a.max_depth + 1 < a.T ? a.max_depth + 1 : a.T);
-  const size_t smem = (size_t)n_max * 2 * a.D * a.elem_bytes;
+  const size_t per_head = (size_t)n_max * 2 * a.D * a.elem_bytes;  // bytes
+  size_t smem = per_head * (size_t)a.Hkv;
+  const size_t cap = 160 * 1024;
+  if (smem > cap) smem = per_head > cap ? per_head : cap / per_head * per_head;
+  CommitParams p = a;
+  p.stage_vecs = (int)(smem / 16);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(commit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  commit_kernel<<<a.B, kThreads, smem, stream>>>(a);
+  commit_kernel<<<a.B, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

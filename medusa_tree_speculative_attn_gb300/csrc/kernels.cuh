@@ -38,6 +38,7 @@ struct AcceptParams {
 
 struct CommitParams {
   int B, T, Hkv, D, P, max_blocks, num_pages, max_depth, rel_width, elem_bytes;
+  int stage_vecs;  // 16-byte entries of the shared staging buffer
   const int* accept_path;
   const int* accept_len;
   void* k_cache;

@@ -4,8 +4,8 @@
 // scratch slots of the paged cache.
 //
 // The tree mask (vLLM issue 1171, void-main: the Medusa tree mask inside the
-// cached-KV attention) is carried as one 64-bit word per node,
-//   anc[i] = anc[parent[i]] | (1 << i),   anc[0] = 1,
+// cached-KV attention) is carried as one 64-bit word per node, the set of the
+// node's ancestors and itself (equivalently anc[i] = anc[parent[i]] | (1 << i)),
 // so node i sees tree key t exactly when bit t of anc[i] is set.  Keys are
 // rotated at position L_b + depth[i] (TensorRT-LLM issue 1946, position
 // offsets for Medusa tokens); keys land at logical slot L_b + i, queries in a
@@ -17,6 +17,34 @@ namespace mt {
 namespace {
 
 constexpr int kPrepThreads = 256;
+
+// 8 consecutive act-dtype elements as one aligned vector.
+template <typename T> struct Vec8 {
+  struct type { uint4 a, b; };  // fp32: 32 bytes
+  static __device__ __forceinline__ type load(const T* p) {
+    const uint4* q = reinterpret_cast<const uint4*>(p);
+    return type{q[0], q[1]};
+  }
+  static __device__ __forceinline__ void store(T* p, const type& v) {
+    uint4* q = reinterpret_cast<uint4*>(p);
+    q[0] = v.a;
+    q[1] = v.b;
+  }
+};
+template <> struct Vec8<__half> {
+  using type = uint4;
+  static __device__ __forceinline__ type load(const __half* p) { return *reinterpret_cast<const uint4*>(p); }
+  static __device__ __forceinline__ void store(__half* p, const type& v) { *reinterpret_cast<uint4*>(p) = v; }
+};
+template <> struct Vec8<__nv_bfloat16> {
+  using type = uint4;
+  static __device__ __forceinline__ type load(const __nv_bfloat16* p) {
+    return *reinterpret_cast<const uint4*>(p);
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const type& v) {
+    *reinterpret_cast<uint4*>(p) = v;
+  }
+};
 
 // Exclusive scan of n values with one block; returns the total.
 __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
@@ -57,29 +85,62 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
 template <typename T>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
   const int tid = threadIdx.x;
-  if (blockIdx.x == gridDim.x - 1) {
-    // ---- schedule block: validate trees, ancestor masks, tile prefix ----
+  if (blockIdx.x == 0) {
+    // ---- schedule block (block 0: dispatched first): validate trees, ancestor masks, tile prefix ----
+    // One warp per sequence; lane l owns nodes l and l + 32.  Ancestor sets by
+    // pointer jumping in shared memory: start from {i} and the parent link,
+    // then six rounds of  anc[i] |= anc[up[i]], up[i] = up[up[i]]  close them
+    // for any depth < 64.
     extern __shared__ int s_nt[];  // [B + 1]
     __shared__ int s_warp[32];
-    for (int b = tid; b < a.B; b += blockDim.x) {
+    __shared__ unsigned long long s_anc[kPrepThreads / 32][kMaxTree];
+    __shared__ int s_up[kPrepThreads / 32][kMaxTree];
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int b = warp; b < a.B; b += kPrepThreads / 32) {
       const int* par = a.tree_parents + (size_t)b * a.T;
       const int* dep = a.tree_depths + (size_t)b * a.T;
-      unsigned long long* anc = a.anc + (size_t)b * a.T;
-      bool ok = par[0] == -1 && dep[0] == 0;
-      unsigned long long m0 = 1ull;
-      anc[0] = m0;
-      for (int i = 1; i < a.T; ++i) {
-        int p = par[i];
-        bool good = p >= 0 && p < i && dep[i] == dep[p] + 1;
-        ok = ok && good;
-        anc[i] = good ? (anc[p] | (1ull << i)) : 0ull;
+      bool good = true;
+      for (int i = lane; i < a.T; i += 32) {
+        const int p = par[i];
+        const bool ok_i = i == 0 ? (p == -1 && dep[0] == 0)
+                                 : (p >= 0 && p < i && dep[i] == dep[p] + 1);
+        good = good && ok_i;
+        s_anc[warp][i] = 1ull << i;
+        s_up[warp][i] = ok_i ? p : -1;
       }
-      int L = a.seq_lens[b];
-      bool len_ok = L >= 0 && (long long)L + a.T <= (long long)a.max_blocks * a.P;
-      if (!ok) set_status(a.status, kStTree);
-      if (!len_ok) set_status(a.status, kStPages);
-      if (!ok || !len_ok) anc[0] = 0ull;  // marks the sequence invalid
-      s_nt[b] = (ok && len_ok) ? (L + a.T + kTileKeys - 1) / kTileKeys : 0;
+      const bool ok = __all_sync(0xffffffffu, good);
+      __syncwarp();
+      for (int round = 0; round < 6; ++round) {
+        unsigned long long na[2];
+        int nu[2];
+        for (int k = 0; k < 2; ++k) {
+          const int i = lane + 32 * k;
+          if (i < a.T) {
+            const int u = s_up[warp][i];
+            na[k] = s_anc[warp][i] | (u >= 0 ? s_anc[warp][u] : 0ull);
+            nu[k] = u >= 0 ? s_up[warp][u] : -1;
+          }
+        }
+        __syncwarp();
+        for (int k = 0; k < 2; ++k) {
+          const int i = lane + 32 * k;
+          if (i < a.T) {
+            s_anc[warp][i] = na[k];
+            s_up[warp][i] = nu[k];
+          }
+        }
+        __syncwarp();
+      }
+      const int L = a.seq_lens[b];
+      const bool len_ok = L >= 0 && (long long)L + a.T <= (long long)a.max_blocks * a.P;
+      for (int i = lane; i < a.T; i += 32)
+        a.anc[(size_t)b * a.T + i] = (ok && len_ok) ? s_anc[warp][i] : 0ull;  // 0 marks invalid
+      if (lane == 0) {
+        if (!ok) set_status(a.status, kStTree);
+        if (!len_ok) set_status(a.status, kStPages);
+        s_nt[b] = (ok && len_ok) ? (L + a.T + kTileKeys - 1) / kTileKeys : 0;
+      }
+      __syncwarp();
     }
     __syncthreads();
     int total = block_exclusive_scan(s_nt, a.B, s_warp);
@@ -87,64 +148,93 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
     if (tid == 0) a.tile_pfx[a.B] = total;
     return;
   }
-  // ---- one warp per row: B*T*Hq query rows, then B*T*Hkv key/value rows ----
-  const int warp = tid >> 5, lane = tid & 31;
-  long long row = (long long)blockIdx.x * (kPrepThreads / 32) + warp;
+  // ---- rotations: B*T*Hq query rows, then B*T*Hkv key/value rows ----
+  // A row is handled by D/16 lanes; lane k rotates the pairs (j, j + D/2) for
+  // j in [8k, 8k + 8) with 16-byte (8-element) loads and stores.
+  const int lanes_per_row = a.D / 16;
+  const int rows_per_warp = 32 / lanes_per_row;
+  const int lane = tid & 31;
+  const int sub = lane / lanes_per_row, k = lane % lanes_per_row;
   const long long nq = (long long)a.B * a.T * a.Hq;
   const long long nk = (long long)a.B * a.T * a.Hkv;
-  if (row >= nq + nk) return;
-  const bool is_q = row < nq;
-  if (!is_q) row -= nq;
-  const int H = is_q ? a.Hq : a.Hkv;
-  const int i = (int)((row / H) % a.T);
-  const int b = (int)(row / ((long long)H * a.T));
-  const int L = a.seq_lens[b];
-  const int depth = a.tree_depths[(size_t)b * a.T + i];
-  const long long pos = (long long)L + depth;
-  if (L < 0 || depth < 0 || pos >= a.max_pos) {
-    if (lane == 0) set_status(a.status, L < 0 ? kStPages : kStTree);
-    return;
-  }
+  const long long nwarps = (long long)(gridDim.x - 1) * (kPrepThreads / 32);
   const int half = a.D / 2;
-  const float2* cs = a.rope + (size_t)pos * half;
-  const T* src;
-  T* dst;
-  if (is_q) {
-    src = static_cast<const T*>(a.q) + (size_t)row * a.D;
-    dst = static_cast<T*>(a.q_rot) + (size_t)row * a.D;
-  } else {
-    const int kvh = (int)(row % a.Hkv);
-    const long long slot = (long long)L + i;
-    if (slot / a.P >= a.max_blocks) {
-      if (lane == 0) set_status(a.status, kStPages);
-      return;
+  for (long long row0 = ((long long)(blockIdx.x - 1) * (kPrepThreads / 32) + (tid >> 5)) * rows_per_warp;
+       row0 < nq + nk; row0 += nwarps * rows_per_warp) {
+    long long row = row0 + sub;
+    if (row >= nq + nk) continue;
+    const bool is_q = row < nq;
+    if (!is_q) row -= nq;
+    const int H = is_q ? a.Hq : a.Hkv;
+    const int i = (int)((row / H) % a.T);
+    const int b = (int)(row / ((long long)H * a.T));
+    const int L = a.seq_lens[b];
+    const int depth = a.tree_depths[(size_t)b * a.T + i];
+    const long long pos = (long long)L + depth;
+    if (L < 0 || depth < 0 || pos >= a.max_pos) {
+      if (k == 0) set_status(a.status, L < 0 ? kStPages : kStTree);
+      continue;
     }
-    const int page = a.block_tables[(size_t)b * a.max_blocks + slot / a.P];
-    if (page < 0 || page >= a.num_pages) {
-      if (lane == 0) set_status(a.status, kStPages);
-      return;
+    const T* src;
+    T* dst;
+    if (is_q) {
+      src = static_cast<const T*>(a.q) + (size_t)row * a.D;
+      dst = static_cast<T*>(a.q_rot) + (size_t)row * a.D;
+    } else {
+      const int kvh = (int)(row % a.Hkv);
+      const long long slot = (long long)L + i;
+      const int page = slot / a.P < a.max_blocks ? a.block_tables[(size_t)b * a.max_blocks + slot / a.P] : -1;
+      if (page < 0 || page >= a.num_pages) {
+        if (k == 0) set_status(a.status, kStPages);
+        continue;
+      }
+      const size_t off = (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * a.D;
+      src = static_cast<const T*>(a.k_new) + (size_t)row * a.D;
+      dst = static_cast<T*>(a.k_cache) + off;
+      // raw value: this lane's two 8-element chunks
+      const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
+      T* vc = static_cast<T*>(a.v_cache) + off;
+      Vec8<T>::store(vc + 8 * k, Vec8<T>::load(vn + 8 * k));
+      Vec8<T>::store(vc + half + 8 * k, Vec8<T>::load(vn + half + 8 * k));
     }
-    const size_t off = (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * a.D;
-    src = static_cast<const T*>(a.k_new) + (size_t)row * a.D;
-    dst = static_cast<T*>(a.k_cache) + off;
-    const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
-    T* vc = static_cast<T*>(a.v_cache) + off;
-    for (int j = lane; j < a.D; j += 32) vc[j] = vn[j];
-  }
-  for (int j = lane; j < half; j += 32) {
-    const float2 c = cs[j];
-    float olo, ohi;
-    rope_pair(Act<T>::to_f(src[j]), Act<T>::to_f(src[j + half]), c.x, c.y, olo, ohi);
-    dst[j] = Act<T>::from_f(olo);
-    dst[j + half] = Act<T>::from_f(ohi);
+    const typename Vec8<T>::type lo_raw = Vec8<T>::load(src + 8 * k);
+    const typename Vec8<T>::type hi_raw = Vec8<T>::load(src + half + 8 * k);
+    const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * half + 8 * k);
+    T lo[8], hi[8], olo[8], ohi[8];
+    memcpy(lo, &lo_raw, sizeof(lo));
+    memcpy(hi, &hi_raw, sizeof(hi));
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float4 c = cs[e / 2];  // (cos, sin) of pairs e and e + 1
+      float l0, h0, l1, h1;
+      rope_pair(Act<T>::to_f(lo[e]), Act<T>::to_f(hi[e]), c.x, c.y, l0, h0);
+      rope_pair(Act<T>::to_f(lo[e + 1]), Act<T>::to_f(hi[e + 1]), c.z, c.w, l1, h1);
+      olo[e] = Act<T>::from_f(l0);
+      olo[e + 1] = Act<T>::from_f(l1);
+      ohi[e] = Act<T>::from_f(h0);
+      ohi[e + 1] = Act<T>::from_f(h1);
+    }
+    typename Vec8<T>::type wl, wh;
+    memcpy(&wl, olo, sizeof(olo));
+    memcpy(&wh, ohi, sizeof(ohi));
+    Vec8<T>::store(dst + 8 * k, wl);
+    Vec8<T>::store(dst + half + 8 * k, wh);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream) {
-  long long nrows = (long long)a.B * a.T * ((long long)a.Hq + a.Hkv);
-  long long blocks = (nrows + kPrepThreads / 32 - 1) / (kPrepThreads / 32) + 1;
+  const long long nrows = (long long)a.B * a.T * ((long long)a.Hq + a.Hkv);
+  const long long rows_per_block = (long long)(kPrepThreads / 32) * (32 / (a.D / 16));
+  int sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long blocks = (nrows + rows_per_block - 1) / rows_per_block;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  if (blocks < 1) blocks = 1;
+  blocks += 1;  // block 0 builds the schedule
   size_t smem = sizeof(int) * (size_t)(a.B + 1);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
   dim3 grid((unsigned)blocks);

@@ -76,6 +76,29 @@ def test_accept_named_configs(name):
     assert st2 == 0 and np.array_equal(alen2, alen) and np.array_equal(path2, path)
 
 
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_accept_special_rows(dt):
+    # all equal (ties everywhere), all -inf, max only in the last element, max
+    # in a later 16-element chunk of a long fp32 row, signed zeros
+    V = 40000
+    rows = []
+    rows.append(np.zeros(V, np.float32))
+    rows.append(np.full(V, -np.inf, np.float32))
+    r = np.full(V, -1.0, np.float32); r[-1] = 2.0; rows.append(r)
+    r = np.full(V, -3.0, np.float32); r[33000] = 1.5; r[39999] = 1.5; rows.append(r)
+    r = np.full(V, -0.0, np.float32); r[7] = 0.0; rows.append(r)
+    r = np.random.default_rng(0).standard_normal(V).astype(np.float32); rows.append(r)
+    T = len(rows)
+    logits = oracle.round_to_act(np.stack(rows)[None], dt)
+    parents = np.array([[-1] + list(range(T - 1))], np.int32)
+    tokens = np.zeros((1, T), np.int32)
+    st, am, alen, path, nxt, _ = _accept_dev(tokens, logits, dt, parents, T - 1)
+    o = oracle.accept_greedy(tokens, logits, dt, parents, T - 1)
+    assert st == 0
+    assert np.array_equal(am, o[0]), (am, o[0])
+    assert np.array_equal(alen, o[1]) and np.array_equal(path, o[2]) and np.array_equal(nxt, o[3])
+
+
 def test_accept_rejects_bad_parents_without_fault():
     tokens = np.zeros((2, 4), np.int32)
     parents = np.array([[-1, 0, 1, 2], [-1, 2, 0, 1]], np.int32)   # second: parent after child
