@@ -43,7 +43,7 @@ int select_kernel(const mt_attn_desc* d) {
 
 struct WsLayout {
   size_t anc, pfx, qrot, ml, o, total;
-  int rows, rows_per_group, nrg, G, nslots;
+  int rows, rows_per_group, part_rows, nrg, G, nslots;
 };
 
 int device_sm_count(int* sms) {
@@ -62,6 +62,7 @@ int layout_for(const mt_attn_desc* d, int kernel, WsLayout* w) {
   w->rows = d->tree_size * g;
   w->rows_per_group = kernel == MT_KERNEL_SIMT ? kSimtRows : kTcRows;
   w->nrg = (w->rows + w->rows_per_group - 1) / w->rows_per_group;
+  w->part_rows = w->rows < w->rows_per_group ? w->rows : w->rows_per_group;
   w->G = sms * (kernel == MT_KERNEL_SIMT ? kSimtCtasPerSm : kTcCtasPerSm);
   const long long nseg = (long long)d->batch * d->num_kv_heads * w->nrg;
   const long long nslots = d->num_splits > 0 ? nseg * d->num_splits : nseg + w->G;
@@ -76,9 +77,9 @@ int layout_for(const mt_attn_desc* d, int kernel, WsLayout* w) {
   off = align_up(off + (size_t)elem_bytes(d->dtype) * d->batch * d->tree_size * d->num_q_heads *
                            d->head_dim);
   w->ml = off;
-  off = align_up(off + sizeof(float2) * (size_t)nslots * w->rows_per_group);
+  off = align_up(off + sizeof(float2) * (size_t)nslots * w->part_rows);
   w->o = off;
-  off = align_up(off + sizeof(float) * (size_t)nslots * w->rows_per_group * d->head_dim);
+  off = align_up(off + sizeof(float) * (size_t)nslots * w->part_rows * d->head_dim);
   w->total = off;
   return MT_OK;
 }
@@ -212,7 +213,7 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   ap.B = d->batch; ap.T = d->tree_size; ap.Hq = d->num_q_heads; ap.Hkv = d->num_kv_heads;
   ap.D = d->head_dim; ap.P = d->page_size; ap.max_blocks = d->max_blocks_per_seq;
   ap.num_pages = d->num_pages; ap.g = d->num_q_heads / d->num_kv_heads;
-  ap.rows = w.rows; ap.rows_per_group = w.rows_per_group;
+  ap.rows = w.rows; ap.rows_per_group = w.rows_per_group; ap.part_rows = w.part_rows;
   const float scale = d->sm_scale > 0.f ? d->sm_scale : (float)(1.0 / std::sqrt((double)d->head_dim));
   ap.scale_log2 = scale * 1.4426950408889634f;
   ap.q_rot = ws + w.qrot; ap.k_cache = k_cache; ap.v_cache = v_cache;

@@ -184,9 +184,9 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
           const int col = tx + 16 * c;
-          dst[(((size_t)pc.slot * (D / 4) + col / 4) * R + r) * 4 + col % 4] = o[i][c];
+          dst[(((size_t)pc.slot * (D / 4) + col / 4) * a.part_rows + r) * 4 + col % 4] = o[i][c];
         }
-        if (tx == 0) a.part_ml[(size_t)pc.slot * R + r] = make_float2(m[i], l[i]);
+        if (tx == 0) a.part_ml[(size_t)pc.slot * a.part_rows + r] = make_float2(m[i], l[i]);
       }
     }
     __syncthreads();

@@ -477,17 +477,17 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
             }
           } else {
             // [slot][D/4][rows]: consecutive rows (threads) write consecutive 16 B
-            float4* dst = a.part_o + ((size_t)pc.slot * C4 + 16 * hh) * kTcRows + seg_row;
+            float4* dst = a.part_o + ((size_t)pc.slot * C4 + 16 * hh) * a.part_rows + seg_row;
 #pragma unroll
             for (int c = 0; c < 16; ++c)
-              dst[(size_t)c * kTcRows] =
+              dst[(size_t)c * a.part_rows] =
                   make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
                               __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
           }
         }
       }
       if (row_ok && pc.slot >= 0)
-        a.part_ml[(size_t)pc.slot * kTcRows + seg_row] = make_float2(m_run, l_run);
+        a.part_ml[(size_t)pc.slot * a.part_rows + seg_row] = make_float2(m_run, l_run);
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(o_free);

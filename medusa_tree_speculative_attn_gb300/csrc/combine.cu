@@ -58,7 +58,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int r = row0 + lane;
-  const bool row_ok = r < RG && rg * RG + r < a.rows;
+  const int PR = a.part_rows;
+  const bool row_ok = r < PR && rg * RG + r < a.rows;
   for (int k0 = 0; k0 < count; k0 += kMaxListed) {
     // list the pieces [k0, k0 + kMaxListed) that exist
     if (tid == 0) s_count = 0;
@@ -80,14 +81,14 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
       for (int k = 0; k < n; ++k) {
         const int slot = s_slot[k];
         if (slot < 0) continue;
-        const float2 ml = a.part_ml[(size_t)slot * RG + r];
+        const float2 ml = a.part_ml[(size_t)slot * PR + r];
         if (ml.x == -INFINITY) continue;  // the piece saw no key of this row
         const float m_new = fmaxf(M, ml.x);
         const float c_old = exp2f(M - m_new), c_new = exp2f(ml.x - m_new);
         lsum = lsum * c_old + ml.y * c_new;
 #pragma unroll
         for (int e = 0; e < PER; ++e) {
-          const float4 v = a.part_o[((size_t)slot * C4 + warp + kWarps * e) * RG + r];
+          const float4 v = a.part_o[((size_t)slot * C4 + warp + kWarps * e) * PR + r];
           acc[e].x = acc[e].x * c_old + v.x * c_new;
           acc[e].y = acc[e].y * c_old + v.y * c_new;
           acc[e].z = acc[e].z * c_old + v.z * c_new;
@@ -113,7 +114,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
     const int lr = idx / CH, ch = idx % CH;
     const int rr = row0 + lr;
     const int row = rg * RG + rr;
-    if (rr >= RG || row >= a.rows) continue;
+    if (rr >= PR || row >= a.rows) continue;
     const int node = row / a.g, h = kvh * a.g + row % a.g;
     T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
     reinterpret_cast<uint4*>(dst)[ch] = *reinterpret_cast<const uint4*>(&s_out[lr][ch * (16 / sizeof(T))]);
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
 template <typename T, int D>
 cudaError_t launch_t(const AttnParams& a, cudaStream_t stream) {
   const int nseg = a.B * a.Hkv * a.sched.nrg;
-  dim3 grid(nseg, (a.rows_per_group + 31) / 32);
+  dim3 grid(nseg, (a.part_rows + 31) / 32);
   combine_kernel<T, D><<<grid, kWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }

@@ -165,7 +165,8 @@ struct PieceIter {
 struct AttnParams {
   int B, T, Hq, Hkv, D, P, max_blocks, num_pages, g;
   int rows;            // T * g query rows per (b, kvh)
-  int rows_per_group;  // RG
+  int rows_per_group;  // RG: query rows per segment (row group)
+  int part_rows;       // rows per partial slot: min(rows, RG)
   float scale_log2;    // sm_scale * log2(e)
   const void* q_rot;   // [B][T][Hq][D] act, rotated and rounded (written by prep)
   const void* k_cache;
@@ -176,8 +177,8 @@ struct AttnParams {
   void* out;
   int* status;
   const unsigned long long* anc;  // [B][T]
-  float4* part_o;                 // [slots][D/4][RG]: unnormalised O, 4 columns per entry
-  float2* part_ml;                // [slots][RG] (max in log2 units, sum)
+  float4* part_o;                 // [slots][D/4][part_rows]: unnormalised O, 4 columns per entry
+  float2* part_ml;                // [slots][part_rows] (max in log2 units, sum)
   Sched sched;
 };
 
