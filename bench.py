@@ -46,6 +46,27 @@ def parse():
     return ap.parse_args()
 
 
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling, no data exchange)."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time (identity for one rank)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Units processed by all ranks per second of the slowest rank."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
             int(os.environ.get("LOCAL_RANK", "0")))
@@ -114,6 +135,32 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def ncu_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of the tensor-core attention kernel from the
+    committed ncu summary, or None when that capture does not describe the
+    kernel as it is now (different workload, kernel or source)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}.md")
+    if kernel == "simt" or not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(("|", "#", "`")):
+            k, _, v = line.partition(":")
+            fields[k.strip()] = v.strip()
+    csrc = os.path.join(ROOT, "medusa_tree_speculative_attn_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("attn_tc.cu", "tc_ptx.cuh", "common.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def algorithmic_bytes(w_host: dict) -> dict:
     """Bytes the path must move at least once (per step)."""
     es = {"f32": 4, "f16": 2, "bf16": 2}[w_host["dtype"]]
@@ -140,7 +187,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    w = workloads.generate(args.workload, seed=args.seed + 1000 * rank, backend="torch", device=str(dev))
+    w = workloads.generate(args.workload, seed=rank_seed(args.seed, rank), backend="torch", device=str(dev))
     spec = w["spec"]
     B, T, md = w["B"], w["T"], w["max_depth"]
     stream = torch.cuda.current_stream()
@@ -261,11 +308,7 @@ def run_ours(args, rank, world, local_rank):
     if st != 0 or (has_accept and mt.read_status(aws) != 0):
         raise RuntimeError(f"device status {st} after timed steps")
     ms = float(np.mean(step_ms))
-    t_max = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(ms, world, dev)
 
     # end to end through the public API with host buffers: pinned H2D of the
     # step's inputs, the three calls, D2H of the step's results
@@ -294,12 +337,8 @@ def run_ours(args, rank, world, local_rank):
             if k >= 2:
                 eev[k - 2][1].record(stream)
         torch.cuda.synchronize()
-        e2e_ms = float(np.mean([a.elapsed_time(b) for a, b in eev]))
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * B * T / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
+        e2e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in eev])), world, dev)
+        e2e = {"value": whole_job_rate(B * T, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
     ab = algorithmic_bytes(w)
@@ -310,10 +349,10 @@ def run_ours(args, rank, world, local_rank):
         achieved = ab["attn"] / (main_avg * 1e-3) / 1e9
         roofline = {"kernel": "tree attention main kernel", "bound": "hbm", "achieved": achieved,
                     "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": None, "ms_per_launch": main_avg,
+                    "traffic": ncu_traffic(args.workload, args.kernel), "ms_per_launch": main_avg,
                     "alg_bytes_per_launch": ab["attn"]}
     res = {
-        "metric": METRIC, "value": world * B * T / (t_max * 1e-3), "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": whole_job_rate(B * T, world, t_max), "unit": UNIT, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": t_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": spec.dtype, "data": "synthetic (seeded)",
         "config": {"workload": args.workload, "batch": B, "tree_nodes": T, "q_heads": w["Hq"],
@@ -324,9 +363,9 @@ def run_ours(args, rank, world, local_rank):
                    "launch": "one CUDA graph per step" if graph is not None else "kernel by kernel",
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "kv_gbs": ab["prefix_kv"] / (main_avg * 1e-3) / 1e9 if main_avg else None,
-        "accepted_tokens_per_s": world * accepted / (t_max * 1e-3) if has_accept else None,
+        "accepted_tokens_per_s": whole_job_rate(accepted, world, t_max) if has_accept else None,
         "alg_bytes": ab, "roofline": roofline, "breakdown": breakdown, "e2e": e2e, "clocks": clocks,
-        "gpu_launches": K * (5 if has_accept else 3), "wall_s_timed_region": wall,
+        "gpu_launches": K * (6 if has_accept else 3), "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_s)
