@@ -148,6 +148,33 @@ int mt_tree_attn_paged(const mt_attn_desc* desc, const void* q, const void* k_ne
                        const mt_rope* rope, void* out, void* workspace, size_t ws_bytes,
                        cudaStream_t stream);
 
+/* ---- Tree attention without allocation -------------------------------------
+ * The pages this library follows have no counterpart for this call.  It is for
+ * callers that cannot allocate device memory on the calling path -- for
+ * example a serving loop that must not risk the device synchronisation and
+ * out-of-memory failures of cudaMalloc between steps, or code that is handed
+ * only its input and output buffers by a memory pool it does not own.
+ * Same computation, arguments and layouts as mt_tree_attn_paged, but no
+ * workspace argument: the workspace is a fixed 64 MiB array that the library
+ * reserves on every device it is loaded on, held until the process exits.
+ *  - Returns MT_ERR_UNSUPPORTED when mt_tree_attn_workspace_size(desc) exceeds
+ *    64 MiB (e.g. very large batches; use mt_tree_attn_paged there).
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *    first call before any stream capture.
+ *  - All calls on one device share the array: calls that overlap on the GPU
+ *    race, so issue them on one stream or order them with events.
+ *  - Each call clears the array's device status word first; if device_status
+ *    is not NULL (a device int32), the status after this call's kernels is
+ *    copied there on `stream` (MT_OK or the device-detected error). */
+int mt_tree_attn_paged_noalloc(const mt_attn_desc* desc, const void* q, const void* k_new,
+                               const void* v_new, void* k_cache, void* v_cache,
+                               const int32_t* block_tables, const int32_t* seq_lens,
+                               const int32_t* tree_parents, const int32_t* tree_depths,
+                               const mt_rope* rope, void* out, int32_t* device_status,
+                               cudaStream_t stream);
+
 /* ---- Greedy acceptance ----------------------------------------------------
  * Per sequence b (LM head at temperature 0):
  *   argmax_out[b][i] = argmax_v target_logits[b][i][v], the lowest index among
