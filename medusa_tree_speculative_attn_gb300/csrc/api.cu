@@ -224,6 +224,10 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   ap.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   ap.sched.B = d->batch; ap.sched.T = d->tree_size; ap.sched.Hkv = d->num_kv_heads;
   ap.sched.nrg = w.nrg; ap.sched.G = w.G; ap.sched.splits = d->num_splits;
+  // fixed work of a piece in tile units: the tensor-core kernel streams a
+  // tile in about 1 us and spends about 4 us on a piece's queries, epilogue
+  // and pipeline refill; the SIMT kernel's tiles are far slower
+  ap.sched.seg_cost = kernel == MT_KERNEL_SIMT ? 1 : 4;
   ap.sched.tile_pfx = pp.tile_pfx;
   const bool prof = g_prof_n < g_prof_cap;
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);

@@ -11,10 +11,13 @@
 // Persistent CTAs (one per SM) walk the balanced schedule of common.cuh.  A
 // CTA holds up to 256 query rows (two 128-row M tiles) of one segment and
 // streams its 64-slot key tiles.  Warp roles:
-//   producer   TMA loads: per piece the rotated queries (one 128-row x 64-col
-//              box per M tile and half), per tile the four 16-slot pages of K
-//              and V (page ids from the block table, 128-byte swizzle; absent
-//              pages use an out-of-range row, which TMA fills with zeros);
+//   producers  four warps, one per SM sub-partition; producer p issues the TMA
+//              loads of page p of every tile (K and V, 128-byte swizzle, page
+//              ids from the block table; absent pages use an out-of-range row,
+//              which TMA fills with zeros).  A single issuing thread cannot
+//              keep HBM busy with 2 KB boxes; four can.  Producer 0 also loads
+//              each piece's rotated queries (one 128-row x 64-col box per M
+//              tile and half);
 //   QK issuer  one thread issues S = Q K^T (M 128, N 64, K D) into TMEM;
 //   PV issuer  one thread issues O += P V (M 128, N D, K 64), P read from
 //              TMEM; separate from the QK issuer so that neither waits behind
@@ -60,10 +63,14 @@ struct Cfg {
   static constexpr int STAGES = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = 1024 + kQBytes + STAGES * kStageBytes + kBarBytes;
   static constexpr int kSoftmaxWarps = 4 * MT;
-  static constexpr int kProducerWarp = kSoftmaxWarps;
-  static constexpr int kQkWarp = kSoftmaxWarps + 1;
-  static constexpr int kPvWarp = kSoftmaxWarps + 2;
-  static constexpr int kThreads = (kSoftmaxWarps + 3) * 32;
+  static constexpr int kQkWarp = kSoftmaxWarps;
+  static constexpr int kPvWarp = kSoftmaxWarps + 1;
+  // four producer warps, one per SM sub-partition (warp w runs on w % 4):
+  // producer p loads page p of each tile's four
+  static constexpr int kProducer0 = kSoftmaxWarps + 2;
+  static constexpr int kProducers = kTileKeys / 16;
+  static constexpr int kProducerBytes = 2 * NH * 16 * 128;  // K and V of one page
+  static constexpr int kThreads = (kSoftmaxWarps + 2 + kProducers) * 32;
   static constexpr int kTmemCols = pow2_at_least(MT * (D + 2 * kTileKeys));
   static_assert(STAGES >= 2, "shared memory budget");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -152,7 +159,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&full[s], C::kProducers);
       tc::mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -171,7 +178,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     tc::tmem_alloc(tmem_slot, C::kTmemCols);
     tc::tmem_relinquish();
   }
-  if (warp == C::kProducerWarp && lane == 0) {
+  if (warp == C::kProducer0 && lane == 0) {
     tc::prefetch_tmap(&tmap_k);
     tc::prefetch_tmap(&tmap_v);
     tc::prefetch_tmap(&tmap_q);
@@ -182,24 +189,28 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const uint32_t sQ_u = tc::smem_u32(sQ), sKV_u = tc::smem_u32(sKV);
 
-  if (warp == C::kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      const uint64_t policy = tc::policy_evict_first();
-      const uint64_t q_policy = tc::policy_evict_last();
-      const int oob_row = a.num_pages * a.Hkv * a.P;
-      const int nodes_per_tile = 128 / a.g;
-      PieceIter pi;
-      pi.init(a.sched, blockIdx.x);
-      Piece pc;
-      uint32_t it = 0, npieces = 0;
-      bool ok = true;
-      while (ok && pi.next(pc)) {
-        // this piece's queries, once every Q K^T of the previous piece is done
-        if (npieces > 0) {
-          ok = tc::mbar_wait(q_empty, (npieces - 1) & 1, abort_flag, a.status);
-          if (!ok) break;
-        }
+  if (warp >= C::kProducer0) {
+    // ----------------------------------------------------------- producers
+    // Each producer warp walks the schedule (page ids fetched warp-wide ahead
+    // of use) and its lane 0 issues the K and V copies of its page of every
+    // tile: one thread's TMA issue rate cannot keep up with HBM, four can.
+    // Producer 0 also loads each piece's queries once the previous piece's
+    // Q K^T are done, without holding back its K/V copies meanwhile.
+    const int pid = warp - C::kProducer0;
+    const uint64_t policy = tc::policy_evict_first();
+    const uint64_t q_policy = tc::policy_evict_last();
+    const int oob_row = a.num_pages * a.Hkv * a.P;
+    PieceIter pi;
+    pi.init(a.sched, blockIdx.x);
+    Piece pc;
+    uint32_t it = 0, npieces = 0, nq = 0;
+    bool ok = true;
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      bool r = tc::mbar_wait(bar, parity, abort_flag, a.status);
+      ok = __all_sync(0xffffffffu, r) && ok;
+    };
+    auto issue_q = [&]() {
+      if (lane == 0) {
         tc::mbar_arrive_expect_tx(q_full, C::kQBytes);
         for (int m = 0; m < MT; ++m) {
           const int z = pc.b * a.T + (pc.rg * kTcRows + m * 128) / a.g;
@@ -207,44 +218,74 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
             tc::tma_load_3d(sQ + (m * C::NH + h) * (128 * 128), &tmap_q, h * 64, pc.kvh * a.g, z,
                             q_full, q_policy);
         }
-        (void)nodes_per_tile;
-        ++npieces;
-        const int nkeys = a.seq_lens[pc.b] + a.T;
-        const int* bt = a.block_tables + (size_t)pc.b * a.max_blocks;
-        for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
-          // page ids of the tile's four pages (fetched before the ring wait)
-          int y[kTileKeys / 16];
-#pragma unroll
-          for (int p = 0; p < kTileKeys / 16; ++p) {
-            const int slot0 = j * kTileKeys + p * 16;
-            y[p] = slot0 < nkeys ? __ldg(bt + slot0 / 16) : -1;
-          }
-          const uint32_t stage = it % S;
-          if (it >= (uint32_t)S) {
-            ok = tc::mbar_wait(&empty[stage], ((it / S) - 1) & 1, abort_flag, a.status);
+      }
+      ++nq;
+    };
+    while (ok && pi.next(pc)) {
+      bool q_pending = pid == 0;
+      if (q_pending && npieces == 0) {
+        issue_q();
+        q_pending = false;
+      }
+      const uint32_t it_first = it;
+      const int nkeys = a.seq_lens[pc.b] + a.T;
+      PageWindow pw;
+      pw.init(a.block_tables + (size_t)pc.b * a.max_blocks, nkeys, a.max_blocks,
+              pc.tile_begin * (kTileKeys / 16), lane);
+      for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
+        const int y = pw.page(j * (kTileKeys / 16) + pid, lane);
+        const uint32_t stage = it % S;
+        if (q_pending) {
+          // the stage about to be refilled held a tile of this piece, whose
+          // P.V needs this piece's Q: load it now; otherwise only if the
+          // previous piece's Q K^T are already done
+          bool ready;
+          if (it >= (uint32_t)S && it - S >= it_first) {
+            wait_all(q_empty, (npieces - 1) & 1);
             if (!ok) break;
+            ready = true;
+          } else {
+            ready = __shfl_sync(0xffffffffu, (int)tc::mbar_try_wait(q_empty, (npieces - 1) & 1), 0) != 0;
           }
-          tc::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-          uint8_t* kdst = sKV + stage * C::kStageBytes;
-          uint8_t* vdst = kdst + C::NH * C::kHalfTile;
-#pragma unroll
-          for (int p = 0; p < kTileKeys / 16; ++p) {
-            int row = oob_row;
-            if (y[p] >= 0 && y[p] < a.num_pages) row = (y[p] * a.Hkv + pc.kvh) * 16;
-            else if (j * kTileKeys + p * 16 < nkeys) set_status(a.status, kStPages);
-#pragma unroll
-            for (int h = 0; h < C::NH; ++h) {
-              tc::tma_load_2d(kdst + h * C::kHalfTile + p * 2048, &tmap_k, h * 64, row, &full[stage], policy);
-              tc::tma_load_2d(vdst + h * C::kHalfTile + p * 2048, &tmap_v, h * 64, row, &full[stage], policy);
-            }
+          if (ready) {
+            issue_q();
+            q_pending = false;
           }
         }
+        if (it >= (uint32_t)S) {
+          wait_all(&empty[stage], ((it / S) - 1) & 1);
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(&full[stage], C::kProducerBytes);
+          uint8_t* kdst = sKV + stage * C::kStageBytes + pid * 2048;
+          uint8_t* vdst = kdst + C::NH * C::kHalfTile;
+          int row = oob_row;
+          if (y >= 0 && y < a.num_pages) row = (y * a.Hkv + pc.kvh) * 16;
+          else if (j * kTileKeys + pid * 16 < nkeys) set_status(a.status, kStPages);
+#pragma unroll
+          for (int h = 0; h < C::NH; ++h) {
+            tc::tma_load_2d(kdst + h * C::kHalfTile, &tmap_k, h * 64, row, &full[stage], policy);
+            tc::tma_load_2d(vdst + h * C::kHalfTile, &tmap_v, h * 64, row, &full[stage], policy);
+          }
+        }
+        __syncwarp();
       }
-      // no TMA load may still be writing shared memory when the CTA exits
+      if (!ok) break;
+      if (q_pending) {
+        wait_all(q_empty, (npieces - 1) & 1);
+        if (!ok) break;
+        issue_q();
+      }
+      ++npieces;
+    }
+    // no TMA load may still be writing shared memory when the CTA exits
+    if (lane == 0) {
       const uint32_t first = it > (uint32_t)S ? it - S : 0;
       for (uint32_t t = first; t < it; ++t) drain_wait(&full[t % S], (t / S) & 1, a.status);
-      if (npieces > 0) drain_wait(q_full, (npieces - 1) & 1, a.status);
+      if (nq > 0) drain_wait(q_full, (nq - 1) & 1, a.status);
     }
+    __syncwarp();
   } else if (warp == C::kQkWarp) {
     // ---------------------------------------------------------- QK issuer
     PieceIter pi;

@@ -41,9 +41,10 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
   int slot0, count;
   long long t0 = 0, W = 0;
   if (s.splits == 0) {
-    W = sched_total_tiles(s);
+    W = sched_total_cost(s);  // balanced mode works in cost units
     t0 = (long long)s.tile_pfx[b] * HR + (long long)seg_in_b * nt;
-    const int c0 = sched_cta_of(t0, W, s.G), c1 = sched_cta_of(t0 + nt - 1, W, s.G);
+    const int c0 = sched_cta_of(sched_tile_cost(s, t0, seg), W, s.G);
+    const int c1 = sched_cta_of(sched_tile_cost(s, t0 + nt - 1, seg), W, s.G);
     if (c0 == c1) return;  // written directly by its only CTA
     slot0 = seg + c0;
     count = c1 - c0 + 1;
@@ -68,7 +69,8 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
       bool exists;
       if (s.splits == 0) {
         const int c = slot0 - seg + k;
-        const long long cb = W * c / s.G, ce = W * (c + 1) / s.G;
+        const long long cb = sched_first_tile_at(s, W * c / s.G);
+        const long long ce = sched_first_tile_at(s, W * (c + 1) / s.G);
         exists = (cb > t0 ? cb : t0) < (ce < t0 + nt ? ce : t0 + nt);
       } else {
         exists = (long long)nt * k / s.splits < (long long)nt * (k + 1) / s.splits;

@@ -54,7 +54,13 @@ __device__ __forceinline__ void rope_pair(float lo, float hi, float c, float s, 
 // number of tiles of one segment of every sequence before b (so sequence b's
 // segments start at tile_pfx[b] * Hkv * nrg).
 //
-// splits == 0 (balanced): CTA c of G takes global tiles [c*W/G, (c+1)*W/G).
+// splits == 0 (balanced): the tiles are dealt out evenly in cost, where a
+//   segment costs its tiles plus seg_cost (the fixed work of starting a
+//   piece: loading its queries, writing its result, refilling the pipeline,
+//   in tile units).  Tile t of segment s sits at cost x(t) = t + seg_cost *
+//   (s + 1); of the total X = W + seg_cost * nseg, CTA c of G takes the tiles
+//   with x in [c*X/G, (c+1)*X/G), a contiguous run of the global list, so a
+//   CTA whose run crosses several short segments gets fewer tiles.
 //   The part of one segment that a CTA takes is a piece; a piece that is a
 //   whole segment writes the output directly, any other piece writes a
 //   partial result to slot s + c (unique: CTAs touching a later segment never
@@ -65,6 +71,7 @@ __device__ __forceinline__ void rope_pair(float lo, float hi, float c, float s, 
 // ---------------------------------------------------------------------------
 struct Sched {
   int B, T, Hkv, nrg, G, splits;
+  int seg_cost;         // balanced mode: per-segment overhead in tile units
   const int* tile_pfx;  // [B + 1]
 };
 
@@ -89,9 +96,40 @@ __device__ __forceinline__ int sched_find_seq(const Sched& s, long long t) {
   return lo;
 }
 
-// CTA that owns global tile t in balanced mode.
-__device__ __forceinline__ int sched_cta_of(long long t, long long W, int G) {
-  return (int)(((t + 1) * (long long)G - 1) / W);
+// Balanced mode: total cost, cost of a global tile, and the first global
+// tile at or past a cost (the total tile count W when there is none).
+__device__ __forceinline__ long long sched_total_cost(const Sched& s) {
+  return sched_total_tiles(s) + (long long)s.seg_cost * s.B * s.Hkv * s.nrg;
+}
+
+__device__ __forceinline__ long long sched_tile_cost(const Sched& s, long long t, long long seg) {
+  return t + (long long)s.seg_cost * (seg + 1);
+}
+
+__device__ __forceinline__ long long sched_first_tile_at(const Sched& s, long long y) {
+  const long long HR = (long long)s.Hkv * s.nrg;
+  // sequence b's segments start at cost tile_pfx[b] * HR + seg_cost * HR * b
+  int lo = 0, hi = s.B - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if ((long long)s.tile_pfx[mid] * HR + (long long)s.seg_cost * HR * mid <= y) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const long long base = (long long)s.tile_pfx[b] * HR + (long long)s.seg_cost * HR * b;
+  const long long nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
+  const long long per = nt + s.seg_cost;  // cost of one segment of sequence b
+  const long long off = y > base ? y - base : 0;
+  if (per == 0) return (long long)s.tile_pfx[b] * HR;
+  const long long k = off / per;
+  if (k >= HR) return (long long)s.tile_pfx[b + 1] * HR;
+  const long long r = off % per;
+  const long long j = r < s.seg_cost ? 0 : r - s.seg_cost;
+  return (long long)s.tile_pfx[b] * HR + k * nt + j;
+}
+
+// CTA whose cost range holds cost x in balanced mode (X the total cost).
+__device__ __forceinline__ int sched_cta_of(long long x, long long X, int G) {
+  return (int)(((x + 1) * (long long)G - 1) / X);
 }
 
 // Iterator over the pieces of one CTA.
@@ -106,8 +144,9 @@ struct PieceIter {
     cta = c;
     if (s.splits == 0) {
       W = sched_total_tiles(s);
-      cur = W * c / s.G;
-      end = W * (c + 1) / s.G;
+      const long long X = sched_total_cost(s);
+      cur = sched_first_tile_at(s, X * c / s.G);
+      end = sched_first_tile_at(s, X * (c + 1) / s.G);
     } else {
       W = (long long)s.B * s.Hkv * s.nrg * s.splits;
       cur = W * c / s.G;
@@ -180,6 +219,39 @@ struct AttnParams {
   float4* part_o;                 // [slots][D/4][part_rows]: unnormalised O, 4 columns per entry
   float2* part_ml;                // [slots][part_rows] (max in log2 units, sum)
   Sched sched;
+};
+
+// Page ids of one sequence's block table as seen by a TMA producer warp.  The
+// warp fetches 32 consecutive entries (eight 64-slot tiles of 16-slot pages)
+// with one coalesced load, and the following 32 are already in flight while
+// the current ones are used, so issuing a tile's copies never waits on a
+// global load.  Entries at or past the sequence's last slot, or past the
+// table's width, read as -1.  Every lane of the warp must call page() with the
+// same, non-decreasing page index.
+struct PageWindow {
+  const int* bt;
+  int nkeys, max_blocks, base, cur, nxt;
+
+  __device__ __forceinline__ int fetch(int first, int lane) const {
+    const int q = first + lane;
+    return (q < max_blocks && q * 16 < nkeys) ? __ldg(bt + q) : -1;
+  }
+  __device__ __forceinline__ void init(const int* bt_, int nkeys_, int max_blocks_, int first_page, int lane) {
+    bt = bt_;
+    nkeys = nkeys_;
+    max_blocks = max_blocks_;
+    base = first_page;
+    cur = fetch(base, lane);
+    nxt = fetch(base + 32, lane);
+  }
+  __device__ __forceinline__ int page(int pg, int lane) {
+    while (pg - base >= 32) {
+      cur = nxt;
+      base += 32;
+      nxt = fetch(base + 32, lane);
+    }
+    return __shfl_sync(0xffffffffu, cur, pg - base);
+  }
 };
 
 }  // namespace mt
