@@ -42,7 +42,7 @@ int select_kernel(const mt_attn_desc* d) {
 }
 
 struct WsLayout {
-  size_t anc, pfx, qrot, ml, o, total;
+  size_t anc, pfx, pieces, qrot, ml, o, total;
   int rows, rows_per_group, part_rows, nrg, G, nslots;
 };
 
@@ -73,6 +73,9 @@ int layout_for(const mt_attn_desc* d, int kernel, WsLayout* w) {
   off = align_up(off + sizeof(unsigned long long) * (size_t)d->batch * d->tree_size);
   w->pfx = off;
   off = align_up(off + sizeof(int) * (size_t)(d->batch + 1));
+  w->pieces = off;  // the tensor-core kernel's per-CTA piece lists
+  if (kernel != MT_KERNEL_SIMT)
+    off = align_up(off + (sizeof(int) + sizeof(PieceRec) * kMaxPieceRecs) * (size_t)w->G);
   w->qrot = off;
   off = align_up(off + (size_t)elem_bytes(d->dtype) * d->batch * d->tree_size * d->num_q_heads *
                            d->head_dim);
@@ -206,6 +209,16 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   pp.rope = rope->table; pp.status = status;
   pp.anc = reinterpret_cast<unsigned long long*>(ws + w.anc);
   pp.tile_pfx = reinterpret_cast<int*>(ws + w.pfx);
+  Sched sched{};
+  sched.B = d->batch; sched.T = d->tree_size; sched.Hkv = d->num_kv_heads;
+  sched.nrg = w.nrg; sched.G = w.G; sched.splits = d->num_splits;
+  // fixed work of a piece in tile units: the tensor-core kernel streams a
+  // tile in about 1 us and spends a few us on a piece's queries, epilogue
+  // and pipeline refill; the SIMT kernel's tiles are far slower
+  sched.seg_cost = kernel == MT_KERNEL_SIMT ? 1 : 4;
+  sched.tile_pfx = pp.tile_pfx;
+  pp.sched = sched;
+  pp.piece_table = kernel == MT_KERNEL_SIMT ? nullptr : reinterpret_cast<int*>(ws + w.pieces);
   st = cuda_status(launch_prep(pp, d->dtype, stream));
   if (st != MT_OK) return st;
 
@@ -222,13 +235,8 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   ap.anc = pp.anc;
   ap.part_o = reinterpret_cast<float4*>(ws + w.o);
   ap.part_ml = reinterpret_cast<float2*>(ws + w.ml);
-  ap.sched.B = d->batch; ap.sched.T = d->tree_size; ap.sched.Hkv = d->num_kv_heads;
-  ap.sched.nrg = w.nrg; ap.sched.G = w.G; ap.sched.splits = d->num_splits;
-  // fixed work of a piece in tile units: the tensor-core kernel streams a
-  // tile in about 1 us and spends about 4 us on a piece's queries, epilogue
-  // and pipeline refill; the SIMT kernel's tiles are far slower
-  ap.sched.seg_cost = kernel == MT_KERNEL_SIMT ? 1 : 4;
-  ap.sched.tile_pfx = pp.tile_pfx;
+  ap.sched = sched;
+  ap.piece_table = pp.piece_table;
   const bool prof = g_prof_n < g_prof_cap;
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);
   if (kernel == MT_KERNEL_SIMT) {

@@ -58,7 +58,7 @@ struct Cfg {
   static constexpr int kQBytes = MT * NH * 128 * 128;   // [m][half][128 rows x 128 B]
   static constexpr int kHalfTile = kTileKeys * 128;     // 64 keys x 128 B
   static constexpr int kStageBytes = 2 * NH * kHalfTile;  // K and V halves
-  static constexpr int kBarBytes = 1024;
+  static constexpr int kBarBytes = 2048;  // barriers (first 1 KB) + the CTA's piece list
   static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kQBytes) / kStageBytes;
   static constexpr int STAGES = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kSmemBytes = 1024 + kQBytes + STAGES * kStageBytes + kBarBytes;
@@ -155,6 +155,9 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   uint64_t* fin = o_free + 1;           // [2] every MMA of each issuer done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* s_npieces = const_cast<int*>(abort_flag + 1);
+  PieceRec* s_pieces = reinterpret_cast<PieceRec*>(reinterpret_cast<uint8_t*>(bars) + 1024);
+  static_assert(kMaxPieceRecs * sizeof(PieceRec) <= C::kBarBytes - 1024, "piece list");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -178,6 +181,14 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     tc::tmem_alloc(tmem_slot, C::kTmemCols);
     tc::tmem_relinquish();
   }
+  if (warp == C::kPvWarp) {
+    // this CTA's piece list (written by the prep kernel) into shared memory
+    const int n = a.piece_table[blockIdx.x];
+    if (lane == 0) *s_npieces = n;
+    const int* src = a.piece_table + a.sched.G + (size_t)blockIdx.x * kMaxPieceRecs * 8;
+    int* dst = reinterpret_cast<int*>(s_pieces);
+    for (int e = lane; e < (n > 0 ? n : 0) * 8; e += 32) dst[e] = src[e];
+  }
   if (warp == C::kProducer0 && lane == 0) {
     tc::prefetch_tmap(&tmap_k);
     tc::prefetch_tmap(&tmap_v);
@@ -200,9 +211,10 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     const uint64_t policy = tc::policy_evict_first();
     const uint64_t q_policy = tc::policy_evict_last();
     const int oob_row = a.num_pages * a.Hkv * a.P;
-    PieceIter pi;
-    pi.init(a.sched, blockIdx.x);
+    PieceSrc pi;
+    pi.init(s_pieces, *s_npieces, a.sched, blockIdx.x, a.seq_lens);
     Piece pc;
+    int pL = 0;
     uint32_t it = 0, npieces = 0, nq = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
@@ -221,14 +233,14 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       }
       ++nq;
     };
-    while (ok && pi.next(pc)) {
+    while (ok && pi.next(pc, pL)) {
       bool q_pending = pid == 0;
       if (q_pending && npieces == 0) {
         issue_q();
         q_pending = false;
       }
       const uint32_t it_first = it;
-      const int nkeys = a.seq_lens[pc.b] + a.T;
+      const int nkeys = pL + a.T;
       PageWindow pw;
       pw.init(a.block_tables + (size_t)pc.b * a.max_blocks, nkeys, a.max_blocks,
               pc.tile_begin * (kTileKeys / 16), lane);
@@ -288,16 +300,17 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     __syncwarp();
   } else if (warp == C::kQkWarp) {
     // ---------------------------------------------------------- QK issuer
-    PieceIter pi;
-    pi.init(a.sched, blockIdx.x);
+    PieceSrc pi;
+    pi.init(s_pieces, *s_npieces, a.sched, blockIdx.x, a.seq_lens);
     Piece pc;
+    int pL = 0;
     uint32_t it = 0, npieces = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       bool r = tc::mbar_wait(bar, parity, abort_flag, a.status);
       ok = __all_sync(0xffffffffu, r) && ok;
     };
-    while (ok && pi.next(pc)) {
+    while (ok && pi.next(pc, pL)) {
       wait_all(q_full, npieces & 1);
       if (!ok) break;
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
@@ -336,17 +349,18 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     __syncwarp();
   } else if (warp == C::kPvWarp) {
     // ---------------------------------------------------------- PV issuer
-    PieceIter pi;
-    pi.init(a.sched, blockIdx.x);
+    PieceSrc pi;
+    pi.init(s_pieces, *s_npieces, a.sched, blockIdx.x, a.seq_lens);
     Piece pc;
+    int pL = 0;
     uint32_t it = 0, npieces = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       bool r = tc::mbar_wait(bar, parity, abort_flag, a.status);
       ok = __all_sync(0xffffffffu, r) && ok;
     };
-    while (ok && pi.next(pc)) {
-      const int nkeys = a.seq_lens[pc.b] + a.T;
+    while (ok && pi.next(pc, pL)) {
+      const int nkeys = pL + a.T;
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
         const uint32_t stage = it % S, buf = it & 1;
         const bool first = j == pc.tile_begin;
@@ -414,16 +428,27 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       bool rr = tc::mbar_wait(bar, parity, abort_flag, a.status);
       ok = __all_sync(0xffffffffu, rr) && ok;
     };
-    PieceIter pi;
-    pi.init(a.sched, blockIdx.x);
+    PieceSrc pi;
+    pi.init(s_pieces, *s_npieces, a.sched, blockIdx.x, a.seq_lens);
     Piece pc;
+    int L = 0;
     uint32_t it = 0;
-    while (ok && pi.next(pc)) {
+    // this row's ancestor mask in piece (b, rg), tmask for rows past the end
+    auto row_anc = [&](int b, int rg) -> unsigned long long {
+      const int row = rg * kTcRows + m * 128 + r;
+      return row < a.rows ? a.anc[(size_t)b * a.T + row / a.g] : tmask;
+    };
+    bool have_next = false;
+    unsigned long long next_anc = 0ull;
+    while (ok && pi.next(pc, L)) {
       const int row = pc.rg * kTcRows + m * 128 + r;
       const bool row_ok = row < a.rows;
       const int node = row_ok ? row / a.g : 0;
-      const unsigned long long anc = row_ok ? a.anc[(size_t)pc.b * a.T + node] : tmask;
-      const int L = a.seq_lens[pc.b];
+      const unsigned long long anc = have_next ? next_anc : row_anc(pc.b, pc.rg);
+      // the next piece's mask is loaded now, long before it is needed
+      const PieceRec* nx = pi.peek();
+      have_next = nx != nullptr;
+      if (have_next) next_anc = row_anc(nx->b, nx->rg);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
         const uint32_t buf = it & 1;
@@ -437,10 +462,17 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         const int k0 = j * kTileKeys;
         if (k0 + kTileKeys > L) {
           // the tile reaches past the prefix: tree mask and sequence end
+          // halves wholly inside the prefix need nothing; only slots of the
+          // tree part take the per-slot test
           const unsigned long long vis = tile_visibility(L, k0, anc);
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (!((vis >> c) & 1ull)) sr[c] = 0xff800000u;  // -inf
+          for (int hw = 0; hw < 2; ++hw) {
+            const uint32_t bits = (uint32_t)(vis >> (32 * hw));
+            if (bits == 0xffffffffu) continue;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (!((bits >> c) & 1u)) sr[32 * hw + c] = 0xff800000u;  // -inf
+          }
         }
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll

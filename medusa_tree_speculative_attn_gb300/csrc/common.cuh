@@ -219,6 +219,55 @@ struct AttnParams {
   float4* part_o;                 // [slots][D/4][part_rows]: unnormalised O, 4 columns per entry
   float2* part_ml;                // [slots][part_rows] (max in log2 units, sum)
   Sched sched;
+  const int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs] (tensor-core kernel)
+};
+
+// A CTA's pieces, listed ahead of time by the prep kernel (up to
+// kMaxPieceRecs; more is recorded as a count of -1), with the sequence's
+// prefix length, so that the attention kernel starts a piece without
+// dependent global loads.  Table layout: int count[G], then
+// PieceRec rec[G][kMaxPieceRecs].
+constexpr int kMaxPieceRecs = 32;
+
+struct PieceRec {
+  int b, kvh, rg, seg, tile_begin, tile_end, slot, L;
+};
+
+// Pieces from a shared-memory copy of the table, or from the schedule itself
+// when the table overflowed (n < 0).
+struct PieceSrc {
+  const PieceRec* rec;
+  int n, idx;
+  PieceIter iter;
+  const int* seq_lens;
+
+  __device__ __forceinline__ void init(const PieceRec* r, int count, const Sched& s, int cta, const int* lens) {
+    rec = r;
+    n = count;
+    idx = 0;
+    seq_lens = lens;
+    if (n < 0) iter.init(s, cta);
+  }
+  __device__ __forceinline__ bool next(Piece& p, int& L) {
+    if (n >= 0) {
+      if (idx >= n) return false;
+      const PieceRec& r = rec[idx++];
+      p.b = r.b;
+      p.kvh = r.kvh;
+      p.rg = r.rg;
+      p.seg = r.seg;
+      p.tile_begin = r.tile_begin;
+      p.tile_end = r.tile_end;
+      p.slot = r.slot;
+      L = r.L;
+      return true;
+    }
+    if (!iter.next(p)) return false;
+    L = seq_lens[p.b];
+    return true;
+  }
+  // The record after the one last returned (table mode only), or null.
+  __device__ __forceinline__ const PieceRec* peek() const { return n >= 0 && idx < n ? &rec[idx] : nullptr; }
 };
 
 // Page ids of one sequence's block table as seen by a TMA producer warp.  The

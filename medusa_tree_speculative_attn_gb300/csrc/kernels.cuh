@@ -21,6 +21,8 @@ struct PrepParams {
   int* status;
   unsigned long long* anc;  // [B][T]
   int* tile_pfx;            // [B + 1]
+  Sched sched;              // the attention kernel's schedule (tile_pfx unused)
+  int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs], or null
 };
 
 struct AcceptParams {

@@ -145,7 +145,36 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
     __syncthreads();
     int total = block_exclusive_scan(s_nt, a.B, s_warp);
     for (int b = tid; b < a.B; b += blockDim.x) a.tile_pfx[b] = s_nt[b];
-    if (tid == 0) a.tile_pfx[a.B] = total;
+    if (tid == 0) {
+      a.tile_pfx[a.B] = total;
+      s_nt[a.B] = total;
+    }
+    if (a.piece_table) {
+      // each CTA's piece list, walked over the prefix in shared memory
+      __syncthreads();
+      Sched sc = a.sched;
+      sc.tile_pfx = s_nt;
+      PieceRec* recs = reinterpret_cast<PieceRec*>(a.piece_table + sc.G);
+      for (int c = tid; c < sc.G; c += blockDim.x) {
+        PieceIter it;
+        it.init(sc, c);
+        Piece p;
+        int n = 0;
+        while (it.next(p)) {
+          if (n == kMaxPieceRecs) {
+            n = -1;
+            break;
+          }
+          PieceRec r;
+          r.b = p.b; r.kvh = p.kvh; r.rg = p.rg; r.seg = p.seg;
+          r.tile_begin = p.tile_begin; r.tile_end = p.tile_end; r.slot = p.slot;
+          r.L = a.seq_lens[p.b];
+          recs[(size_t)c * kMaxPieceRecs + n] = r;
+          ++n;
+        }
+        a.piece_table[c] = n;
+      }
+    }
     return;
   }
   // ---- rotations: B*T*Hq query rows, then B*T*Hkv key/value rows ----
