@@ -56,12 +56,14 @@ template <int D, int MT>
 struct Cfg {
   static constexpr int NH = D / 64;                     // 64-element halves of a head row
   static constexpr int kQBytes = MT * NH * 128 * 128;   // [m][half][128 rows x 128 B]
+  static constexpr int kPTile = 128 * kTileKeys * 2;     // P of one M tile: 128 rows x 128 B
+  static constexpr int kPBytes = MT * kPTile;            // [m]
   static constexpr int kHalfTile = kTileKeys * 128;     // 64 keys x 128 B
   static constexpr int kStageBytes = 2 * NH * kHalfTile;  // K and V halves
   static constexpr int kBarBytes = 2048;  // barriers (first 1 KB) + the CTA's piece list
-  static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kQBytes) / kStageBytes;
+  static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kQBytes - kPBytes) / kStageBytes;
   static constexpr int STAGES = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kSmemBytes = 1024 + kQBytes + STAGES * kStageBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kQBytes + kPBytes + STAGES * kStageBytes + kBarBytes;
   static constexpr int kSoftmaxWarps = 4 * MT;
   static constexpr int kQkWarp = kSoftmaxWarps;
   static constexpr int kPvWarp = kSoftmaxWarps + 1;
@@ -71,15 +73,14 @@ struct Cfg {
   static constexpr int kProducers = kTileKeys / 16;
   static constexpr int kProducerBytes = 2 * NH * 16 * 128;  // K and V of one page
   static constexpr int kThreads = (kSoftmaxWarps + 2 + kProducers) * 32;
-  static constexpr int kTmemCols = pow2_at_least(MT * (D + 2 * kTileKeys));
+  // TMEM: O (D fp32 columns per M tile), S (64 per M tile), Q (D/2 packed
+  // 16-bit pairs per M tile)
+  static constexpr int kTmemCols = pow2_at_least(MT * (D + kTileKeys + D / 2));
   static_assert(STAGES >= 2, "shared memory budget");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
   __device__ static constexpr uint32_t o_col(int m) { return (uint32_t)(m * D); }
-  // S (64 fp32 columns) of tile buffer `buf`, M tile m; P overwrites its
-  // first 32 columns with packed 16-bit pairs.
-  __device__ static constexpr uint32_t s_col(int buf, int m) {
-    return (uint32_t)(MT * D + (buf * MT + m) * kTileKeys);
-  }
+  __device__ static constexpr uint32_t s_col(int m) { return (uint32_t)(MT * D + m * kTileKeys); }
+  __device__ static constexpr uint32_t q_col(int m) { return (uint32_t)(MT * (D + kTileKeys) + m * (D / 2)); }
 };
 
 template <typename T> struct Pack2;
@@ -142,14 +143,17 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sQ = smem;
-  uint8_t* sKV = sQ + C::kQBytes;
+  uint8_t* sP = sQ + C::kQBytes;     // [m] P tiles, 128-byte swizzled, K-major
+  uint8_t* sKV = sP + C::kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
   uint64_t* full = bars;                // [S] K/V stage landed
   uint64_t* empty = full + S;           // [S] K/V stage consumed by its P.V
-  uint64_t* s_full = empty + S;         // [2] S of a tile buffer computed
-  uint64_t* p_full = s_full + 2;        // [2][MT] P written (and O rescaled)
-  uint64_t* pv_done = p_full + 2 * MT;  // [2] O += P V of a tile buffer done
-  uint64_t* q_full = pv_done + 2;       // Q of the current piece landed
+  // per M tile, one phase per tile:
+  uint64_t* s_full = empty + S;         // [MT] S computed
+  uint64_t* p_full = s_full + MT;       // [MT] P written (and O rescaled)
+  uint64_t* pv_done = p_full + MT;      // [MT] O += P V done
+  uint64_t* s_free = pv_done + MT;      // [MT] S read out by the softmax
+  uint64_t* q_full = s_free + MT;       // Q of the current piece landed
   uint64_t* q_empty = q_full + 1;       // every Q K^T of the previous piece done
   uint64_t* o_free = q_empty + 1;       // O of the previous piece read out
   uint64_t* fin = o_free + 1;           // [2] every MMA of each issuer done
@@ -165,12 +169,14 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       tc::mbar_init(&full[s], C::kProducers);
       tc::mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      tc::mbar_init(&s_full[b], 1);
-      tc::mbar_init(&pv_done[b], 1);
-      tc::mbar_init(&fin[b], 1);
-      for (int m = 0; m < MT; ++m) tc::mbar_init(&p_full[b * MT + m], 4);
+    for (int m = 0; m < MT; ++m) {
+      tc::mbar_init(&s_full[m], 1);
+      tc::mbar_init(&p_full[m], 4);
+      tc::mbar_init(&pv_done[m], 1);
+      tc::mbar_init(&s_free[m], 4);
     }
+    tc::mbar_init(&fin[0], 1);
+    tc::mbar_init(&fin[1], 1);
     tc::mbar_init(q_full, 1);
     tc::mbar_init(q_empty, 1);
     tc::mbar_init(o_free, C::kSoftmaxWarps);
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sQ_u = tc::smem_u32(sQ), sKV_u = tc::smem_u32(sKV);
+  const uint32_t sQ_u = tc::smem_u32(sQ), sKV_u = tc::smem_u32(sKV), sP_u = tc::smem_u32(sP);
 
   if (warp >= C::kProducer0) {
     // ----------------------------------------------------------- producers
@@ -311,34 +317,47 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       ok = __all_sync(0xffffffffu, r) && ok;
     };
     while (ok && pi.next(pc, pL)) {
+      // the piece's queries: shared memory -> TMEM (after every Q K^T of the
+      // previous piece, in issue order), then the staging buffer is free
       wait_all(q_full, npieces & 1);
       if (!ok) break;
+      tc::tc_fence_after();
+      if (lane == 0) {
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t h = kk / 4, k4 = kk % 4;
+            tc::tmem_cp_128x256b(tmem + C::q_col(m) + kk * 8,
+                                 tc::smem_desc(sQ_u + (m * C::NH + h) * (128 * 128) + k4 * 32, 16, 1024));
+          }
+        tc::mma_commit(q_empty);
+      }
+      __syncwarp();
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
-        const uint32_t stage = it % S, buf = it & 1;
+        const uint32_t stage = it % S;
         wait_all(&full[stage], (it / S) & 1);
         if (!ok) break;
-        // S[buf] held P of tile it - 2 until its P.V completed
-        if (it >= 2) {
-          wait_all(&pv_done[buf], ((it - 2) >> 1) & 1);
-          if (!ok) break;
-        }
-        tc::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t k_u = sKV_u + stage * C::kStageBytes;
-          for (int m = 0; m < MT; ++m) {
+        const uint32_t k_u = sKV_u + stage * C::kStageBytes;
+        for (int m = 0; m < MT; ++m) {
+          // S_m held the scores of tile it - 1 until the softmax read them
+          if (it >= 1) {
+            wait_all(&s_free[m], (it - 1) & 1);
+            if (!ok) break;
+          }
+          tc::tc_fence_after();
+          if (lane == 0) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t h = kk / 4, k4 = kk % 4;
-              const uint64_t ad = tc::smem_desc(sQ_u + (m * C::NH + h) * (128 * 128) + k4 * 32, 16, 1024);
               const uint64_t bd = tc::smem_desc(k_u + h * C::kHalfTile + k4 * 32, 16, 1024);
-              if (kk == 0) tc::mma_f16_ss<false>(tmem + C::s_col(buf, m), ad, bd, kIdescQK);
-              else tc::mma_f16_ss<true>(tmem + C::s_col(buf, m), ad, bd, kIdescQK);
+              if (kk == 0) tc::mma_f16_ts<false>(tmem + C::s_col(m), tmem + C::q_col(m) + kk * 8, bd, kIdescQK);
+              else tc::mma_f16_ts<true>(tmem + C::s_col(m), tmem + C::q_col(m) + kk * 8, bd, kIdescQK);
             }
+            tc::mma_commit(&s_full[m]);
           }
-          tc::mma_commit(&s_full[buf]);
-          if (j + 1 == pc.tile_end) tc::mma_commit(q_empty);
+          __syncwarp();
         }
-        __syncwarp();
+        if (!ok) break;
       }
       ++npieces;
     }
@@ -362,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     while (ok && pi.next(pc, pL)) {
       const int nkeys = pL + a.T;
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
-        const uint32_t stage = it % S, buf = it & 1;
+        const uint32_t stage = it % S;
         const bool first = j == pc.tile_begin;
         if (first && npieces > 0) {
           wait_all(o_free, (npieces - 1) & 1);
@@ -384,27 +403,28 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         }
         const uint32_t v_u = sKV_u + stage * C::kStageBytes + C::NH * C::kHalfTile;
         for (int m = 0; m < MT; ++m) {
-          wait_all(&p_full[buf * MT + m], (it >> 1) & 1);
+          wait_all(&p_full[m], it & 1);
           if (!ok) break;
           tc::tc_fence_after();
           if (lane == 0) {
-            const uint32_t d_t = tmem + C::o_col(m), a_t = tmem + C::s_col(buf, m);
+            const uint32_t d_t = tmem + C::o_col(m);
+            const uint32_t p_u = sP_u + m * C::kPTile;
             if (first)
-              tc::mma_f16_ts<false>(d_t, a_t, tc::smem_desc(v_u, C::kHalfTile, 1024), kIdescPV);
+              tc::mma_f16_ss<false>(d_t, tc::smem_desc(p_u, 16, 1024), tc::smem_desc(v_u, C::kHalfTile, 1024),
+                                    kIdescPV);
             else
-              tc::mma_f16_ts<true>(d_t, a_t, tc::smem_desc(v_u, C::kHalfTile, 1024), kIdescPV);
+              tc::mma_f16_ss<true>(d_t, tc::smem_desc(p_u, 16, 1024), tc::smem_desc(v_u, C::kHalfTile, 1024),
+                                   kIdescPV);
 #pragma unroll
             for (int kk = 1; kk < kTileKeys / 16; ++kk)
-              tc::mma_f16_ts<true>(d_t, a_t + kk * 8, tc::smem_desc(v_u + kk * 2048, C::kHalfTile, 1024),
-                                   kIdescPV);
+              tc::mma_f16_ss<true>(d_t, tc::smem_desc(p_u + kk * 32, 16, 1024),
+                                   tc::smem_desc(v_u + kk * 2048, C::kHalfTile, 1024), kIdescPV);
+            tc::mma_commit(&pv_done[m]);
           }
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) {
-          tc::mma_commit(&pv_done[buf]);
-          tc::mma_commit(&empty[stage]);
-        }
+        if (lane == 0) tc::mma_commit(&empty[stage]);
         __syncwarp();
       }
       ++npieces;
@@ -451,14 +471,17 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       if (have_next) next_anc = row_anc(nx->b, nx->rg);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
-        const uint32_t buf = it & 1;
-        const uint32_t s_addr = tmem + lane_addr + C::s_col(buf, m);
-        wait_all(&s_full[buf], (it >> 1) & 1);
+        const uint32_t s_addr = tmem + lane_addr + C::s_col(m);
+        wait_all(&s_full[m], it & 1);
         if (!ok) break;
         tc::tc_fence_after();
         uint32_t sr[64];
         tc::tmem_ld_x64(s_addr, sr);
         tc::tmem_ld_wait();
+        // the scores are in registers: S may take the next tile's scores
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&s_free[m]);
         const int k0 = j * kTileKeys;
         if (k0 + kTileKeys > L) {
           // the tile reaches past the prefix: tree mask and sequence end
@@ -500,11 +523,23 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
           rs1 += p1;
           pk[c] = Pack2<T>::pack(p0, p1);
         }
-        tc::tmem_st_x32(s_addr, pk);
-        if (__any_sync(0xffffffffu, need_o)) {
-          // O holds the P.V sum up to tile it - 1: wait for it, then rescale
-          wait_all(&pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1);
+        // P into this M tile's shared-memory buffer, once the P.V of tile
+        // it - 1 (which read it) is done: row r is 128 B (64 keys) in an
+        // 8-row, 128-byte swizzle atom (16-byte chunk c at c ^ (r % 8))
+        if (it >= 1) {
+          wait_all(&pv_done[m], (it - 1) & 1);
           if (!ok) break;
+        }
+        {
+          uint8_t* prow = sP + m * C::kPTile + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          tc::fence_proxy_async_smem();  // visible to the tensor core's reads
+        }
+        if (__any_sync(0xffffffffu, need_o)) {
+          // O holds the P.V sum up to tile it - 1 (done: waited above)
           tc::tc_fence_after();
 #pragma unroll 1
           for (int hh = 0; hh < D / 64; ++hh) {
@@ -521,11 +556,11 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         m_run = m_new;
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&p_full[buf * MT + m]);
+        if (lane == 0) tc::mbar_arrive(&p_full[m]);
       }
       if (!ok) break;
       // epilogue
-      wait_all(&pv_done[(it - 1) & 1], ((it - 1) >> 1) & 1);
+      wait_all(&pv_done[m], (it - 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
       const int seg_row = m * 128 + r;

@@ -266,6 +266,14 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
   }
 }
 
+// Copy a 128-row x 32-byte slice of a shared-memory matrix (described like an
+// MMA operand, swizzle included) into TMEM: row i -> lane i, the 16 16-bit
+// elements -> 8 columns of packed pairs.  Asynchronous; ordered before later
+// tcgen05.mma / tcgen05.commit of the same thread.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this
 // thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
