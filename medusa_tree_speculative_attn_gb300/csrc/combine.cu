@@ -68,10 +68,12 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
     for (int k = k0 + tid; k < count && k < k0 + kMaxListed; k += blockDim.x) {
       bool exists;
       if (s.splits == 0) {
+        // the segment's tiles are one contiguous stretch of the cost axis:
+        // its first and last owners hold tiles of it, and a CTA in between
+        // covers its whole cost range inside it, so it holds tiles exactly
+        // when that range is not empty
         const int c = slot0 - seg + k;
-        const long long cb = sched_first_tile_at(s, W * c / s.G);
-        const long long ce = sched_first_tile_at(s, W * (c + 1) / s.G);
-        exists = (cb > t0 ? cb : t0) < (ce < t0 + nt ? ce : t0 + nt);
+        exists = k == 0 || k == count - 1 || W * (c + 1) / s.G > W * c / s.G;
       } else {
         exists = (long long)nt * k / s.splits < (long long)nt * (k + 1) / s.splits;
       }

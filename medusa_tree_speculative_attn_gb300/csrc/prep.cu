@@ -91,7 +91,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
     // pointer jumping in shared memory: start from {i} and the parent link,
     // then six rounds of  anc[i] |= anc[up[i]], up[i] = up[up[i]]  close them
     // for any depth < 64.
-    extern __shared__ int s_nt[];  // [B + 1]
+    extern __shared__ int s_nt[];  // [B + 1] tiles per segment, then [B] prefix lengths
+    int* s_len = s_nt + a.B + 1;
     __shared__ int s_warp[32];
     __shared__ unsigned long long s_anc[kPrepThreads / 32][kMaxTree];
     __shared__ int s_up[kPrepThreads / 32][kMaxTree];
@@ -133,6 +134,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
       }
       const int L = a.seq_lens[b];
       const bool len_ok = L >= 0 && (long long)L + a.T <= (long long)a.max_blocks * a.P;
+      if (lane == 0) s_len[b] = L;
       for (int i = lane; i < a.T; i += 32)
         a.anc[(size_t)b * a.T + i] = (ok && len_ok) ? s_anc[warp][i] : 0ull;  // 0 marks invalid
       if (lane == 0) {
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
           PieceRec r;
           r.b = p.b; r.kvh = p.kvh; r.rg = p.rg; r.seg = p.seg;
           r.tile_begin = p.tile_begin; r.tile_end = p.tile_end; r.slot = p.slot;
-          r.L = a.seq_lens[p.b];
+          r.L = s_len[p.b];
           recs[(size_t)c * kMaxPieceRecs + n] = r;
           ++n;
         }
@@ -264,7 +266,7 @@ cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream) {
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   if (blocks < 1) blocks = 1;
   blocks += 1;  // block 0 builds the schedule
-  size_t smem = sizeof(int) * (size_t)(a.B + 1);
+  size_t smem = sizeof(int) * (size_t)(2 * a.B + 1);
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
   dim3 grid((unsigned)blocks);
   switch (dtype) {
