@@ -59,6 +59,7 @@ def _load():
             lib.or_tree_scatter.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
                                             P, P, P, P, P, P]
             lib.or_accept_greedy.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+            lib.or_tree_candidates.argtypes = [i32, i32, i32, i32, i32, P, P, P, P]
             lib.or_kv_commit.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                          P, P, P, P, P, P, P, i32]
             _lib = lib
@@ -212,6 +213,20 @@ def accept_greedy(tokens, logits: np.ndarray, logits_dtype: str, parents, max_de
                                   _ptr(nxt))
     _check(st, "accept_greedy")
     return am, alen, path, nxt
+
+
+def tree_candidates(root_logits: np.ndarray, head_logits: np.ndarray, logits_dtype: str, parents):
+    """Returns (tokens [B,T], status): node 0 the argmax of root_logits[b], node i the
+    rank-r entry of head_logits[b][depth_i - 1], r = number of earlier siblings."""
+    parents = _i32(parents)
+    B, T = parents.shape
+    heads, V = head_logits.shape[1], head_logits.shape[2]
+    root = _act(root_logits, logits_dtype)
+    heads_a = _act(head_logits, logits_dtype)
+    tokens = np.full((B, T), -1, np.int32)
+    st = _load().or_tree_candidates(DTYPES[logits_dtype], B, T, heads, V, _ptr(root), _ptr(heads_a),
+                                    _ptr(parents), _ptr(tokens))
+    return tokens, st
 
 
 def released_width(T: int, page_size: int) -> int:

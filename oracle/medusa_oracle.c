@@ -460,3 +460,60 @@ int or_kv_commit(int dt, int B, int T, int Hkv, int D, int P, int max_blocks, in
   }
   return status;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Candidate tree tokens from the base and Medusa-head logits                 */
+/* (lmdeploy PR 1231 "[WIP] support Medusa": generate_candidates; Medusa heads */
+/* at top-k over a 64-choice tree).  Reading: node 0 takes the argmax of the   */
+/* base logits; a node at depth d with r earlier siblings takes the entry of   */
+/* rank r of head d-1, ranked by larger value first, lower index first among   */
+/* equal values.  The entry of rank r is found by r+1 successive selections,   */
+/* each of the best entry ranked after the previous one.                      */
+/* ------------------------------------------------------------------------- */
+
+/* 1 if (v, i) ranks before (w, j). */
+static int ranks_before(double v, int i, double w, int j) {
+  return v > w || (v == w && i < j);
+}
+
+static int rank_entry(int dt, const void* logits, size_t row, int V, int r) {
+  double pv = 0.0;
+  int pi = -1;  /* previous selection; none yet */
+  for (int k = 0; k <= r; ++k) {
+    double bv = 0.0;
+    int bi = -1;
+    for (int v = 0; v < V; ++v) {
+      double x = load_act(dt, logits, row + v);
+      if (pi >= 0 && !ranks_before(pv, pi, x, v)) continue; /* not after the previous one */
+      if (bi < 0 || ranks_before(x, v, bv, bi)) { bv = x; bi = v; }
+    }
+    if (bi < 0) return -1; /* fewer than r+1 entries */
+    pv = bv;
+    pi = bi;
+  }
+  return pi;
+}
+
+int or_tree_candidates(int dt, int B, int T, int heads, int V, const void* root_logits,
+                       const void* head_logits, const int32_t* parents, int32_t* tokens) {
+  if (B < 0 || T < 1 || T > 64 || heads < 1 || V < 1) return OR_ERR_ARG;
+  int status = OR_OK;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parents + (size_t)b * T;
+    if (check_tree(T, par, NULL)) { status = OR_ERR_TREE; continue; }
+    int depth[64];
+    depth[0] = 0;
+    for (int i = 1; i < T; ++i) depth[i] = depth[par[i]] + 1;
+    int bad = 0;
+    for (int i = 0; i < T; ++i) if (depth[i] > heads) bad = 1;
+    if (bad) { status = OR_ERR_TREE; continue; }
+    tokens[(size_t)b * T] = rank_entry(dt, root_logits, (size_t)b * V, V, 0);
+    for (int i = 1; i < T; ++i) {
+      int r = 0;
+      for (int j = 1; j < i; ++j) if (par[j] == par[i]) ++r;
+      size_t row = ((size_t)b * heads + (depth[i] - 1)) * (size_t)V;
+      tokens[(size_t)b * T + i] = rank_entry(dt, head_logits, row, V, r);
+    }
+  }
+  return status;
+}
