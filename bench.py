@@ -161,6 +161,51 @@ def ncu_traffic(workload: str, kernel: str):
         return None
 
 
+def measure_candidates(w: dict, K: int, flush, stream, peak: float) -> dict:
+    """The step before verification (candidate tree tokens from the base logits and
+    the Medusa heads' logits), timed on its own with the workload's trees and
+    max_depth heads: seeded random logits in the workload's logits dtype, L2
+    flushed before every call (outside the events)."""
+    import torch
+    import medusa_tree_speculative_attn_gb300 as mt
+    dev = w["logits"].device
+    B, T, V = w["B"], w["T"], w["vocab"]
+    heads = w["max_depth"] if w["max_depth"] > 0 else 1
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    dt = w["logits"].dtype
+    root = torch.randn((B, V), generator=gen, device=dev, dtype=torch.float32).to(dt)
+    hl = torch.randn((B, heads, V), generator=gen, device=dev, dtype=torch.float32).to(dt)
+    tok = torch.empty((B, T), dtype=torch.int32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    call = lambda: mt.tree_candidates(root, hl, w["tree_parents"], tok, status_ws=ws)
+    # replayed as a CUDA graph, like the step, so that host overhead stays out
+    # of the events
+    gs = torch.cuda.Stream()
+    gs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(gs):
+        for _ in range(3):
+            call()
+    torch.cuda.current_stream().wait_stream(gs)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=gs):
+        call()
+    mk = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [(mk(), mk()) for _ in range(K)]
+    for k in range(K):
+        flush.fill_((k + 7) & 0xFF)
+        ev[k][0].record(stream)
+        graph.replay()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    st = mt.read_status(ws)
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    nbytes = B * (heads + 1) * V * root.element_size() + 2 * B * T * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms_per_call": ms, "alg_bytes": nbytes, "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / peak,
+            "heads": heads, "status": st, "l2": "flushed before each call", "launch": "CUDA graph replay"}
+
+
 def algorithmic_bytes(w_host: dict) -> dict:
     """Bytes the path must move at least once (per step)."""
     es = {"f32": 4, "f16": 2, "bf16": 2}[w_host["dtype"]]
@@ -343,6 +388,7 @@ def run_ours(args, rank, world, local_rank):
 
     ab = algorithmic_bytes(w)
     peak, peak_src = measured_peaks()
+    cand = measure_candidates(w, K, flush, stream, peak) if has_accept else None
     main_avg = float(np.mean(main_ms)) if main_ms else None
     roofline = None
     if main_avg:
@@ -365,6 +411,7 @@ def run_ours(args, rank, world, local_rank):
         "kv_gbs": ab["prefix_kv"] / (main_avg * 1e-3) / 1e9 if main_avg else None,
         "accepted_tokens_per_s": whole_job_rate(accepted, world, t_max) if has_accept else None,
         "alg_bytes": ab, "roofline": roofline, "breakdown": breakdown, "e2e": e2e, "clocks": clocks,
+        "tree_candidates": cand,
         "gpu_launches": K * (6 if has_accept else 3), "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -218,6 +218,36 @@ int mt_kv_commit(const mt_attn_desc* desc, int max_depth, const int32_t* accept_
                  int32_t* block_tables, int32_t* seq_lens, int32_t* released_pages,
                  void* status_ws, cudaStream_t stream);
 
+/* ---- Candidate tree tokens ---------------------------------------------------
+ * The step before verification (lmdeploy PR 1231 "[WIP] support Medusa":
+ * porting `generate_candidates`, Medusa heads at top-k over a 64-choice tree):
+ * the tree's tokens from the base model's logits and the Medusa heads' logits.
+ * For each sequence b, with the tree given by tree_parents[b] (node 0 the
+ * root; parent[0] = -1, 0 <= parent[i] < i):
+ *   tree_tokens[b][0] = argmax_v root_logits[b][v] (lowest index among equal
+ *                       maxima);
+ *   for node i >= 1 at depth d (1 <= d <= heads) with r earlier siblings (nodes
+ *   j < i with the same parent): tree_tokens[b][i] = the entry of rank r
+ *   (0-based) of head_logits[b][d-1], ordered by larger value first and lower
+ *   vocab index first among equal values (+0 and -0 are equal); -1 when the
+ *   head has fewer than r + 1 entries (r >= V).
+ * root_logits [B][V] and head_logits [B][heads][V] in logits_dtype (no NaN);
+ * tree_parents int32 [B][T]; tree_tokens int32 [B][T] out.  The tree template
+ * (which choice of which head each node takes) is thus the tree's own shape:
+ * the r-th child of a node takes the r-th best token of the next head.
+ * Host errors: MT_ERR_INVALID_ARG for null or unaligned pointers or sizes out
+ * of range (heads in [1, 63], V >= 1); MT_ERR_UNSUPPORTED for T outside
+ * [1, 64] or another dtype.  Device status MT_ERR_TREE (in the first int32 of
+ * status_ws, at least 256 bytes, read with mt_read_status): a malformed tree,
+ * a node deeper than `heads`, or a node with 16 or more earlier siblings; the
+ * tokens of that sequence (malformed tree or depth) or of that depth (too many
+ * siblings) are not written.  The pages do not define the tree template; this
+ * rule (child rank = head rank) is the reading used here. */
+int mt_tree_candidates(int batch, int tree_size, int heads, int vocab, mt_dtype logits_dtype,
+                       const void* root_logits, const void* head_logits,
+                       const int32_t* tree_parents, int32_t* tree_tokens, void* status_ws,
+                       cudaStream_t stream);
+
 /* ---- Status ------------------------------------------------------------------
  * Waits for `stream`, then reads and clears the device status word at the start
  * of `workspace` (MT_OK or the first device-side error since the last read). */

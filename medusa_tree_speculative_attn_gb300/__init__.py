@@ -10,6 +10,7 @@ Calls (same names as the C ABI without the ``mt_`` prefix):
   tree_attn_paged    tree tokens attend to the paged prefix + their ancestors
   tree_accept_greedy per-node argmax and the longest matching root path
   kv_commit          move accepted K/V into place, grow lengths, release pages
+  tree_candidates    the tree's tokens from the base and Medusa-head logits
 """
 from __future__ import annotations
 
@@ -66,6 +67,7 @@ def _load():
         lib.mt_tree_accept_workspace_size.restype = Z
         lib.mt_tree_accept_greedy.argtypes = [I, I, I, I, I] + [P] * 8 + [Z, P]
         lib.mt_kv_commit.argtypes = [D, I] + [P] * 8 + [P]
+        lib.mt_tree_candidates.argtypes = [I, I, I, I, I] + [P] * 5 + [P]
         lib.mt_read_status.argtypes = [P, P, ctypes.POINTER(I)]
         lib.mt_profile_enable.argtypes = [I]
         lib.mt_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
@@ -226,6 +228,29 @@ def kv_commit(accept_path, accept_len, k_cache, v_cache, block_tables, seq_lens,
                               _ptr(accept_len), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                               _ptr(seq_lens), _ptr(released_pages), _ptr(status_ws), _stream(stream))
     _check(st, "mt_kv_commit")
+
+
+def tree_candidates(root_logits, head_logits, tree_parents, tree_tokens, *, status_ws: torch.Tensor,
+                    stream=None):
+    """Tree tokens from the base logits [B,V] and the Medusa heads' logits [B,heads,V]:
+    node 0 takes the argmax of the base logits, the r-th child (r earlier siblings)
+    of a depth-(d-1) node the rank-r token of head d-1."""
+    _need(root_logits, "root_logits", None, 2)
+    _need(head_logits, "head_logits", root_logits.dtype, 3)
+    _need(tree_parents, "tree_parents", torch.int32, 2)
+    _need(tree_tokens, "tree_tokens", torch.int32, 2)
+    B, V = root_logits.shape
+    heads = head_logits.shape[1]
+    if head_logits.shape != (B, heads, V):
+        raise ValueError("head_logits must be [B, heads, V]")
+    T = tree_parents.shape[1]
+    if tree_parents.shape != (B, T) or tree_tokens.shape != (B, T):
+        raise ValueError("tree_parents and tree_tokens must be [B, T]")
+    st = _load().mt_tree_candidates(B, T, heads, V, _DTYPES[root_logits.dtype], _ptr(root_logits),
+                                    _ptr(head_logits), _ptr(tree_parents), _ptr(tree_tokens),
+                                    _ptr(status_ws), _stream(stream))
+    _check(st, "mt_tree_candidates")
+    return tree_tokens
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

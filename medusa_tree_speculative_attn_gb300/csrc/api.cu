@@ -316,6 +316,27 @@ int mt_kv_commit(const mt_attn_desc* d, int max_depth, const int32_t* accept_pat
   return cuda_status(launch_commit(c, stream));
 }
 
+int mt_tree_candidates(int batch, int tree_size, int heads, int vocab, mt_dtype logits_dtype,
+                       const void* root_logits, const void* head_logits,
+                       const int32_t* tree_parents, int32_t* tree_tokens, void* status_ws,
+                       cudaStream_t stream) {
+  if (batch < 1 || batch > kMaxBatch || heads < 1 || heads >= kMaxTree || vocab < 1)
+    return MT_ERR_INVALID_ARG;
+  if (tree_size < 1 || tree_size > kMaxTree) return MT_ERR_UNSUPPORTED;
+  if (logits_dtype != MT_F32 && logits_dtype != MT_F16 && logits_dtype != MT_BF16)
+    return MT_ERR_UNSUPPORTED;
+  if (!root_logits || !head_logits || !tree_parents || !tree_tokens || !status_ws)
+    return MT_ERR_INVALID_ARG;
+  if (!aligned16(root_logits) || !aligned16(head_logits) || !aligned16(status_ws))
+    return MT_ERR_INVALID_ARG;
+  CandParams c{};
+  c.B = batch; c.T = tree_size; c.V = vocab; c.heads = heads;
+  c.root_logits = root_logits; c.head_logits = head_logits;
+  c.parents = tree_parents; c.tokens = tree_tokens;
+  c.status = static_cast<int*>(status_ws);
+  return cuda_status(launch_cand(c, logits_dtype, stream));
+}
+
 int mt_profile_enable(int max_records) {
   if (max_records < 0 || max_records > (1 << 16)) return MT_ERR_INVALID_ARG;
   for (int i = 0; i < 2 * g_prof_cap; ++i) cudaEventDestroy(g_prof_ev[i]);

@@ -25,6 +25,18 @@ struct PrepParams {
   int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs], or null
 };
 
+// Candidate tree tokens from the Medusa heads (cand.cu).
+constexpr int kMaxChoices = 16;  // choice ranks per depth the kernel supports
+
+struct CandParams {
+  int B, T, V, heads;
+  const void* root_logits;  // [B][V]
+  const void* head_logits;  // [B][heads][V]
+  const int* parents;       // [B][T]
+  int* tokens;              // [B][T] out
+  int* status;
+};
+
 struct AcceptParams {
   int B, T, V, max_depth;
   const int* tokens;
@@ -69,6 +81,7 @@ bool tc_supported(int D, int g);
 cudaError_t launch_attn_tc(const AttnParams& a, int dtype, const void* tmap_k, const void* tmap_v,
                            const void* tmap_q, cudaStream_t stream);
 cudaError_t launch_combine(const AttnParams& a, int dtype, cudaStream_t stream);
+cudaError_t launch_cand(const CandParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_accept(const AcceptParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& a, cudaStream_t stream);
 

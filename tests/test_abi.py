@@ -28,7 +28,7 @@ def declared_functions():
 
 def test_header_declares_the_three_calls():
     names = declared_functions()
-    for n in ("mt_tree_attn_paged", "mt_tree_accept_greedy", "mt_kv_commit",
+    for n in ("mt_tree_attn_paged", "mt_tree_accept_greedy", "mt_kv_commit", "mt_tree_candidates",
               "mt_tree_attn_workspace_size", "mt_tree_accept_workspace_size", "mt_rope_create",
               "mt_rope_destroy", "mt_read_status", "mt_status_string", "mt_version"):
         assert n in names
@@ -99,6 +99,24 @@ def test_accept_and_commit_reject_bad_sizes(lib):
     assert lib.mt_kv_commit(ctypes.byref(d), 3, p, p, p, p, p, p, p, p, None) == -2
     d = _desc()
     assert lib.mt_kv_commit(ctypes.byref(d), 3, None, p, p, p, p, p, p, p, None) == -1
+
+
+def test_candidates_reject_bad_arguments(lib):
+    P = ctypes.c_void_p
+    buf = (ctypes.c_char * 4096)()
+    p = ctypes.cast(buf, P)
+    c = lib.mt_tree_candidates
+    assert c(1, 65, 2, 10, 0, p, p, p, p, p, None) == -2  # tree larger than 64 nodes
+    assert c(1, 0, 2, 10, 0, p, p, p, p, p, None) == -2
+    assert c(1, 8, 0, 10, 0, p, p, p, p, p, None) == -1  # no heads
+    assert c(1, 8, 64, 10, 0, p, p, p, p, p, None) == -1  # more heads than tree depths
+    assert c(1, 8, 2, 0, 0, p, p, p, p, p, None) == -1  # empty vocab
+    assert c(0, 8, 2, 10, 0, p, p, p, p, p, None) == -1  # empty batch
+    assert c(1, 8, 2, 10, 7, p, p, p, p, p, None) == -2  # unknown dtype
+    for k in range(5):
+        args = [p] * 5
+        args[k] = None
+        assert c(1, 8, 2, 10, 0, *args, None) == -1  # null pointer
 
 
 def test_rope_create_rejects_bad_arguments(lib):
