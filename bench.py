@@ -1,6 +1,8 @@
 """Benchmark of the Medusa tree-verification step on one GB300 (or N replicas).
 
-One step = tree_attn_paged + tree_accept_greedy + kv_commit over one batch of
+One step = tree_attn_paged + tree_accept_commit (greedy acceptance and the KV
+commit in one launch; ``--accept separate`` runs tree_accept_greedy then
+kv_commit instead) over one batch of
 the serving workload (batch 16, 32 q / 8 kv heads, D 128, bf16, prefixes
 uniform in [512, 8192], 64-node trees, bf16 logits over a 32000 vocab), inputs
 resident in HBM.  Between steps (outside the timed events) the block tables and
@@ -43,6 +45,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    ap.add_argument("--accept", default="fused", choices=["fused", "separate"],
+                    help="acceptance and commit in one launch, or as the two calls")
     return ap.parse_args()
 
 
@@ -259,7 +263,11 @@ def run_ours(args, rank, world, local_rank):
         mt.tree_attn_paged(s["q"], w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"],
                            s["tree_parents"], s["tree_depths"], out, k_new=s["k_new"], v_new=s["v_new"],
                            rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel)
-        if has_accept:
+        if has_accept and args.accept == "fused":
+            mt.tree_accept_commit(s["tree_tokens"], s["logits"], s["tree_parents"], alen, path,
+                                  w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
+                                  argmax_out=am, next_token=nxt, workspace=aws)
+        elif has_accept:
             mt.tree_accept_greedy(s["tree_tokens"], s["logits"], s["tree_parents"], alen, path,
                                   argmax_out=am, next_token=nxt, workspace=aws)
             mt.kv_commit(path, alen, w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
@@ -277,12 +285,12 @@ def run_ours(args, rank, world, local_rank):
     # (1) kernel-level: per-call events and the main attention kernel's own
     # duration (library profiling hook), kernels launched one by one
     mk = lambda: torch.cuda.Event(enable_timing=True)
-    evb = [(mk(), mk(), mk(), mk()) for _ in range(K)]
+    evb = [(mk(), mk(), mk(), mk(), mk(), mk()) for _ in range(K)]
     mt.profile_enable(K)
     for k in range(K):
         restore()
         flush.fill_(k & 0xFF)
-        e0, e1, e2, e3 = evb[k]
+        e0, e1, e2, e3, e4, e5 = evb[k]
         e0.record(stream)
         mt.tree_attn_paged(w["q"], w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"],
                            w["tree_parents"], w["tree_depths"], out, k_new=w["k_new"], v_new=w["v_new"],
@@ -294,16 +302,28 @@ def run_ours(args, rank, world, local_rank):
             e2.record(stream)
             mt.kv_commit(path, alen, w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
                          tree_size=T, status_ws=ws)
+            e3.record(stream)
+            restore()
+            flush.fill_(k & 0xFF)
+            e4.record(stream)
+            mt.tree_accept_commit(w["tree_tokens"], w["logits"], w["tree_parents"], alen, path,
+                                  w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
+                                  argmax_out=am, next_token=nxt, workspace=aws)
+            e5.record(stream)
         else:
-            e2.record(stream)
-        e3.record(stream)
+            for e in (e2, e3, e4, e5):
+                e.record(stream)
     torch.cuda.synchronize()
     main_ms = mt.profile_read(K)
     mt.profile_enable(0)
-    breakdown = {"tree_attn_paged_ms": float(np.mean([a.elapsed_time(b) for a, b, _, _ in evb])),
+    avg = lambda i, j: float(np.mean([e[i].elapsed_time(e[j]) for e in evb]))
+    breakdown = {"tree_attn_paged_ms": avg(0, 1),
                  "attention_main_kernel_ms": float(np.mean(main_ms)) if main_ms else None,
-                 "tree_accept_greedy_ms": float(np.mean([b.elapsed_time(c) for _, b, c, _ in evb])),
-                 "kv_commit_ms": float(np.mean([c.elapsed_time(d) for _, _, c, d in evb]))}
+                 "tree_accept_greedy_ms": avg(1, 2), "kv_commit_ms": avg(2, 3),
+                 "tree_accept_commit_ms": avg(4, 5),
+                 "note": "each call timed alone, L2 flushed before the attention and before the "
+                         "fused call; the step uses " + ("tree_accept_commit" if args.accept == "fused"
+                                                          else "tree_accept_greedy + kv_commit")}
 
     # (2) the timed steps: the whole step replayed as one CUDA graph (or
     # launched kernel by kernel with --no-graph)
@@ -356,7 +376,7 @@ def run_ours(args, rank, world, local_rank):
     t_max = max_over_ranks(ms, world, dev)
 
     # end to end through the public API with host buffers: pinned H2D of the
-    # step's inputs, the three calls, D2H of the step's results
+    # step's inputs, the step's calls, D2H of the step's results
     e2e = None
     if not args.no_e2e:
         keys_in = ["q", "k_new", "v_new", "tree_parents", "tree_depths"]
@@ -405,14 +425,15 @@ def run_ours(args, rank, world, local_rank):
                    "kv_heads": w["Hkv"], "head_dim": w["head_dim"], "page_size": w["page_size"],
                    "prefix": list(spec.prefix), "logits": (f"{w['logits_dtype']} vocab {w['vocab']}"
                                                            if has_accept else None),
-                   "kernel": args.kernel, "num_splits": args.splits,
+                   "kernel": args.kernel, "num_splits": args.splits, "accept": args.accept,
                    "launch": "one CUDA graph per step" if graph is not None else "kernel by kernel",
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "kv_gbs": ab["prefix_kv"] / (main_avg * 1e-3) / 1e9 if main_avg else None,
         "accepted_tokens_per_s": whole_job_rate(accepted, world, t_max) if has_accept else None,
         "alg_bytes": ab, "roofline": roofline, "breakdown": breakdown, "e2e": e2e, "clocks": clocks,
         "tree_candidates": cand,
-        "gpu_launches": K * (6 if has_accept else 3), "wall_s_timed_region": wall,
+        "gpu_launches": K * (3 + (0 if not has_accept else 1 if args.accept == "fused" else 2)),
+        "wall_s_timed_region": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_s)

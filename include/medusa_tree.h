@@ -13,7 +13,9 @@
  *                         argmax;
  *   mt_kv_commit          the accepted nodes' K/V move into the sequence's next
  *                         cache slots, the sequence length grows and the tree
- *                         scratch pages past the new length are released.
+ *                         scratch pages past the new length are released;
+ *
+ * or in two, with mt_tree_accept_commit doing the last two in one launch.
  *
  * What the pages fix, per call:
  *  - vLLM issue 1171 "[Discussion] Will vLLM consider using Speculative
@@ -217,6 +219,26 @@ int mt_kv_commit(const mt_attn_desc* desc, int max_depth, const int32_t* accept_
                  const int32_t* accept_len, void* k_cache, void* v_cache,
                  int32_t* block_tables, int32_t* seq_lens, int32_t* released_pages,
                  void* status_ws, cudaStream_t stream);
+
+/* ---- Greedy acceptance and KV commit in one launch ---------------------------
+ * The composition mt_tree_accept_greedy then mt_kv_commit (same results, same
+ * arguments and layouts as those two calls), as one kernel launch: each
+ * sequence is committed as soon as its path is known, by the CTA that
+ * completed its argmax rows, so the step has no launch or round trip between
+ * acceptance and commit.  desc supplies B (batch), T (tree_size), Hkv, D, P,
+ * max_blocks_per_seq, num_pages and the cache dtype; the logits have their own
+ * dtype.  workspace: mt_tree_accept_workspace_size(B, T) bytes, zero-filled
+ * before first use; its first int32 is the device status word, which records
+ * the acceptance errors (MT_ERR_TREE) and the commit errors (MT_ERR_PAGES) of
+ * both calls.  Host errors: those of the two calls.  A sequence whose tree is
+ * malformed or too deep is accepted as the root alone (accept_len 0) and
+ * committed so, exactly as the two calls would do. */
+int mt_tree_accept_commit(const mt_attn_desc* desc, int vocab, int max_depth, mt_dtype logits_dtype,
+                          const int32_t* tree_tokens, const void* target_logits,
+                          const int32_t* tree_parents, int32_t* argmax_out, int32_t* accept_len,
+                          int32_t* accept_path, int32_t* next_token, void* k_cache, void* v_cache,
+                          int32_t* block_tables, int32_t* seq_lens, int32_t* released_pages,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- Candidate tree tokens ---------------------------------------------------
  * The step before verification (lmdeploy PR 1231 "[WIP] support Medusa":

@@ -10,6 +10,7 @@ Calls (same names as the C ABI without the ``mt_`` prefix):
   tree_attn_paged    tree tokens attend to the paged prefix + their ancestors
   tree_accept_greedy per-node argmax and the longest matching root path
   kv_commit          move accepted K/V into place, grow lengths, release pages
+  tree_accept_commit the last two in one launch
   tree_candidates    the tree's tokens from the base and Medusa-head logits
 """
 from __future__ import annotations
@@ -67,6 +68,7 @@ def _load():
         lib.mt_tree_accept_workspace_size.restype = Z
         lib.mt_tree_accept_greedy.argtypes = [I, I, I, I, I] + [P] * 8 + [Z, P]
         lib.mt_kv_commit.argtypes = [D, I] + [P] * 8 + [P]
+        lib.mt_tree_accept_commit.argtypes = [D, I, I, I] + [P] * 12 + [P, Z, P]
         lib.mt_tree_candidates.argtypes = [I, I, I, I, I] + [P] * 5 + [P]
         lib.mt_read_status.argtypes = [P, P, ctypes.POINTER(I)]
         lib.mt_profile_enable.argtypes = [I]
@@ -228,6 +230,43 @@ def kv_commit(accept_path, accept_len, k_cache, v_cache, block_tables, seq_lens,
                               _ptr(accept_len), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                               _ptr(seq_lens), _ptr(released_pages), _ptr(status_ws), _stream(stream))
     _check(st, "mt_kv_commit")
+
+
+def tree_accept_commit(tree_tokens, target_logits, tree_parents, accept_len, accept_path, k_cache,
+                       v_cache, block_tables, seq_lens, released_pages, *, argmax_out, next_token,
+                       workspace: torch.Tensor, max_depth: Optional[int] = None, stream=None):
+    """tree_accept_greedy followed by kv_commit, in one launch (same results)."""
+    _need(tree_tokens, "tree_tokens", torch.int32, 2)
+    _need(tree_parents, "tree_parents", torch.int32, 2)
+    _need(target_logits, "target_logits", None, 3)
+    for name, t in (("accept_len", accept_len), ("next_token", next_token), ("seq_lens", seq_lens)):
+        _need(t, name, torch.int32, 1)
+    for name, t in (("accept_path", accept_path), ("argmax_out", argmax_out),
+                    ("block_tables", block_tables), ("released_pages", released_pages)):
+        _need(t, name, torch.int32, 2)
+    _need(k_cache, "k_cache", None, 4)
+    _need(v_cache, "v_cache", k_cache.dtype, 4)
+    _need(workspace, "workspace")
+    B, T = tree_tokens.shape
+    V = target_logits.shape[2]
+    if max_depth is None:
+        max_depth = accept_path.shape[1] - 1
+    if accept_path.shape[1] != max_depth + 1:
+        raise ValueError("accept_path must have max_depth + 1 columns")
+    num_pages, Hkv, P, D = k_cache.shape
+    if released_pages.shape != (B, released_width(T, P)):
+        raise ValueError("released_pages must be [B, (T + 2P - 2) // P]")
+    desc = AttnDesc(B, int(T), Hkv, Hkv, D, P, block_tables.shape[1], num_pages, 0,
+                    _DTYPES[k_cache.dtype], 0.0, 0)
+    st = _load().mt_tree_accept_commit(ctypes.byref(desc), V, int(max_depth),
+                                       _DTYPES[target_logits.dtype], _ptr(tree_tokens),
+                                       _ptr(target_logits), _ptr(tree_parents), _ptr(argmax_out),
+                                       _ptr(accept_len), _ptr(accept_path), _ptr(next_token),
+                                       _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       _ptr(seq_lens), _ptr(released_pages), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "mt_tree_accept_commit")
+    return accept_len, accept_path
 
 
 def tree_candidates(root_logits, head_logits, tree_parents, tree_tokens, *, status_ws: torch.Tensor,

@@ -1,16 +1,17 @@
 // Greedy acceptance (LM head at temperature 0; lmdeploy PR 1231 "[WIP] support
 // Medusa" -- the `evaluate_posterior` step -- and vLLM issue 1171, "it uses
-// the argmax result").
+// the argmax result"), optionally fused with the KV commit.
 //
-// Two kernels: the per-node argmax over the vocab (values compared exactly;
-// +0 and -0 are equal; a larger value wins, the lower index among equal
-// values), streamed through shared memory by persistent CTAs; then one warp
-// per sequence selects the path:
+// One launch: a CTA per node takes the argmax over the vocab of its logits row
+// (values compared exactly; +0 and -0 are equal; a larger value wins, the
+// lower index among equal values), publishes it and counts itself in its
+// sequence's arrival counter.  The CTA that completes a sequence resets the
+// counter and selects the path with one warp:
 //   acc[0] = 1, acc[i] = acc[parent[i]] && token[i] == argmax[parent[i]],
 //   end = the deepest accepted node (lowest index among equals),
-// and writes accept_len, the padded root-to-end path and next_token.
-#include "kernels.cuh"
-#include "tc_ptx.cuh"
+// writes accept_len, the padded root-to-end path and next_token, and, in the
+// fused form, commits the sequence's K/V (commit_seq.cuh) right away.
+#include "commit_seq.cuh"
 
 namespace mt {
 
@@ -45,12 +46,6 @@ template <> struct Max8<float> {  // 4 values per vector for fp32
   }
 };
 
-constexpr int kChunkBytes = 32 * 1024;
-constexpr int kStages = 6;
-constexpr int kVecsPerChunk = kChunkBytes / 16;
-constexpr int kStreamThreads = 512;
-constexpr int kStreamWarps = kStreamThreads / 32;
-
 __device__ __forceinline__ void warp_best(float& best, int& bidx) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -60,159 +55,62 @@ __device__ __forceinline__ void warp_best(float& best, int& bidx) {
   }
 }
 
-// Per-node argmax.  Persistent CTAs take rows r = blockIdx.x, + gridDim.x, ...
-// and stream them in 32 KB chunks through a 6-stage shared-memory ring filled
-// by 1-D bulk copies (thread 0 issues; an mbarrier per stage counts bytes).
-// Each thread scans its 16-byte vectors in increasing index order keeping
-// (max, first index): a vector's packed maximum is compared first and the
-// vector is searched only when it beats the running maximum.  At the end of a
-// row each warp leaves its (max, index) in shared memory and warp 0 merges
-// them after the chunk barrier, so rows cost no extra block synchronisation.
-template <typename T>
-__global__ void __launch_bounds__(kStreamThreads) argmax_stream_kernel(AcceptParams a) {
-  constexpr int EPV = 16 / sizeof(T);
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint4* ring = reinterpret_cast<uint4*>(smem);  // [kStages][kVecsPerChunk]
-  __shared__ uint64_t full[kStages];
-  __shared__ float s_pv[2][kStreamWarps];
-  __shared__ int s_pi[2][kStreamWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const long long row_bytes = (long long)a.V * sizeof(T);
-  const int chunks_per_row = (int)((row_bytes + kChunkBytes - 1) / kChunkBytes);
-  const int nrows = a.B * a.T;
-  const int my_rows = blockIdx.x < nrows ? (nrows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-  const long long total = (long long)my_rows * chunks_per_row;
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) tc::mbar_init(&full[s], 1);
-    tc::fence_barrier_init();
-  }
-  __syncthreads();
-  const uint64_t policy = tc::policy_evict_first();
-  auto issue = [&](long long k) {  // chunk k of this CTA into stage k % kStages
-    const int row = blockIdx.x + (int)(k / chunks_per_row) * gridDim.x;
-    const long long off = (k % chunks_per_row) * (long long)kChunkBytes;
-    const uint32_t bytes = (uint32_t)min((long long)kChunkBytes, row_bytes - off);
-    uint64_t* bar = &full[k % kStages];
-    tc::mbar_arrive_expect_tx(bar, bytes);
-    tc::bulk_load(ring + (k % kStages) * kVecsPerChunk,
-                  static_cast<const uint8_t*>(a.logits) + (size_t)row * row_bytes + off, bytes, bar, policy);
-  };
-  long long issued = 0;  // chunks handed to the copy engine (thread 0)
-  if (tid == 0) {
-    for (long long k = 0; k < total && k < kStages; ++k) issue(k);
-    issued = total < kStages ? total : kStages;
-  }
-  volatile int no_abort = 0;
-  float best = -INFINITY;
-  int bidx = 0x7fffffff;
-  bool ok = true;
-  for (long long k = 0; k < total; ++k) {
-    const int stage = (int)(k % kStages);
-    if (ok) ok = tc::mbar_wait(&full[stage], (uint32_t)((k / kStages) & 1), &no_abort, a.status);
-    const int c = (int)(k % chunks_per_row);
-    const int rowi = (int)(k / chunks_per_row);
-    const long long off = (long long)c * kChunkBytes;
-    const int nvec = (int)(min((long long)kChunkBytes, row_bytes - off) / 16);
-    const uint4* chunk = ring + stage * kVecsPerChunk;
-    if (ok) {
-      const int base = (int)(off / 16);
-      for (int v = tid; v < nvec; v += kStreamThreads) {
-        const uint4 raw = chunk[v];
-        const float m = Max8<T>::of(raw);
-        if (m > best || bidx == 0x7fffffff) {
-          T tmp[EPV];
-          memcpy(tmp, &raw, 16);
-#pragma unroll
-          for (int e = EPV - 1; e >= 0; --e)
-            if (Act<T>::to_f(tmp[e]) == m) bidx = (base + v) * EPV + e;
-          best = m;
-        }
-      }
-    }
-    const bool row_end = c == chunks_per_row - 1;
-    if (row_end) {
-      warp_best(best, bidx);
-      if (lane == 0) {
-        s_pv[rowi & 1][warp] = best;
-        s_pi[rowi & 1][warp] = bidx;
-      }
-      best = -INFINITY;
-      bidx = 0x7fffffff;
-    }
-    __syncthreads();  // stage consumed; row results (if any) published
-    if (tid == 0 && ok && k + kStages < total) {
-      issue(k + kStages);
-      issued = k + kStages + 1;
-    }
-    if (row_end && warp == 0) {
-      // merge the row's warp results; their slots are rewritten two rows
-      // later, after further chunk barriers that warp 0 must also reach
-      float v = lane < kStreamWarps ? s_pv[rowi & 1][lane] : -INFINITY;
-      int ix = lane < kStreamWarps ? s_pi[rowi & 1][lane] : 0x7fffffff;
-      warp_best(v, ix);
-      if (lane == 0) a.argmax_out[blockIdx.x + rowi * gridDim.x] = ix;
-    }
-  }
-  // after a timed-out wait: no bulk copy may still target shared memory at exit
-  if (tid == 0)
-    for (long long k = issued > kStages ? issued - kStages : 0; k < issued; ++k) {
-      const uint64_t t0 = tc::global_timer_ns();
-      while (!tc::mbar_try_wait(&full[k % kStages], (uint32_t)((k / kStages) & 1)) &&
-             tc::global_timer_ns() - t0 < tc::kWaitLimitNs) {
-      }
-    }
-}
+// Shared state of a sequence's path selection (one warp) and commit.
+struct FinishSmem {
+  unsigned long long anc[kMaxTree];
+  int up[kMaxTree], dep[kMaxTree], am[kMaxTree];
+  int par[kMaxTree], tok[kMaxTree];  // the sequence's tree and tokens
+  int path[kMaxTree];
+  int len;      // accepted length
+  int seq_len;  // seq_lens[b] before the commit
+  int last;
+  CommitSmem commit;
+};
 
-// Fallback for rows that are not 16-byte aligned: one CTA per row, scalar loads.
-template <typename T>
-__global__ void __launch_bounds__(kThreads) argmax_scalar_kernel(AcceptParams a) {
-  __shared__ float s_v[kThreads / 32];
-  __shared__ int s_i[kThreads / 32];
-  const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const T* lg = static_cast<const T*>(a.logits) + (size_t)row * a.V;
-  float best = -INFINITY;
-  int bidx = 0x7fffffff;
-  for (int v = threadIdx.x; v < a.V; v += kThreads) {
-    const float x = Act<T>::to_f(lg[v]);
-    if (better(x, v, best, bidx)) { best = x; bidx = v; }
+// The sequence's parents, tokens and (for the commit) length, loaded by every
+// row's CTA at its start so that their latency hides behind the row's logits;
+// only the CTA that completes the sequence uses them.
+struct SeqPrefetch {
+  int par, tok, len;
+  __device__ __forceinline__ void load(const AcceptParams& a, const CommitParams& c, int b, bool commit) {
+    const int t = threadIdx.x;
+    par = t < a.T ? a.parents[(size_t)b * a.T + t] : 0;
+    tok = t < a.T ? a.tokens[(size_t)b * a.T + t] : 0;
+    len = commit && t == 0 ? c.seq_lens[b] : 0;
   }
-  warp_best(best, bidx);
-  if (lane == 0) { s_v[warp] = best; s_i[warp] = bidx; }
-  __syncthreads();
-  if (warp == 0) {
-    float v = lane < kThreads / 32 ? s_v[lane] : -INFINITY;
-    int ix = lane < kThreads / 32 ? s_i[lane] : 0x7fffffff;
-    warp_best(v, ix);
-    if (lane == 0) a.argmax_out[row] = ix;
+  __device__ __forceinline__ void store(const AcceptParams& a, FinishSmem& sm) const {
+    const int t = threadIdx.x;
+    if (t < a.T) {
+      sm.par[t] = par;
+      sm.tok[t] = tok;
+    }
+    if (t == 0) sm.seq_len = len;
   }
-}
+};
 
-// Greedy path, one warp per sequence, every step in parallel over the nodes
+// Greedy path of sequence b by one warp, every step in parallel over the nodes
 // (lane l owns nodes l and l + 32):
 //   ancestors and depths by pointer jumping (six rounds close any depth < 64);
 //   node i matches when tokens[i] == argmax[parent[i]] (the root always);
 //   node i is accepted when every node on its root path matches;
 //   end = the accepted node of largest depth, the lowest index among equals.
-constexpr int kPathWarps = 8;
-__global__ void __launch_bounds__(kPathWarps * 32) accept_path_kernel(AcceptParams a) {
-  __shared__ unsigned long long s_anc[kPathWarps][kMaxTree];
-  __shared__ int s_up[kPathWarps][kMaxTree], s_dep[kPathWarps][kMaxTree], s_am[kPathWarps][kMaxTree];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.x * kPathWarps + warp;
-  if (b >= a.B) return;
+// The argmax values were written by other CTAs: read through L2.  Parents and
+// tokens come from shared memory (SeqPrefetch).
+__device__ void select_path(const AcceptParams& a, int b, FinishSmem& sm) {
+  const int lane = threadIdx.x & 31;
   const int T = a.T;
-  const int* par = a.parents + (size_t)b * T;
-  const int* tok = a.tokens + (size_t)b * T;
+  const int* par = sm.par;
+  const int* tok = sm.tok;
   const int* am = a.argmax_out + (size_t)b * T;
   bool good = true;
   for (int i = lane; i < T; i += 32) {
     const int p = par[i];
     const bool ok_i = i == 0 ? p == -1 : (p >= 0 && p < i);
     good = good && ok_i;
-    s_anc[warp][i] = 1ull << i;
-    s_up[warp][i] = (i > 0 && ok_i) ? p : -1;
-    s_dep[warp][i] = (i > 0 && ok_i) ? 1 : 0;
-    s_am[warp][i] = am[i];
+    sm.anc[i] = 1ull << i;
+    sm.up[i] = (i > 0 && ok_i) ? p : -1;
+    sm.dep[i] = (i > 0 && ok_i) ? 1 : 0;
+    sm.am[i] = __ldcg(am + i);
   }
   const bool ok = __all_sync(0xffffffffu, good);
   __syncwarp();
@@ -222,19 +120,19 @@ __global__ void __launch_bounds__(kPathWarps * 32) accept_path_kernel(AcceptPara
     for (int k = 0; k < 2; ++k) {
       const int i = lane + 32 * k;
       if (i < T) {
-        const int u = s_up[warp][i];
-        na[k] = s_anc[warp][i] | (u >= 0 ? s_anc[warp][u] : 0ull);
-        nd[k] = s_dep[warp][i] + (u >= 0 ? s_dep[warp][u] : 0);
-        nu[k] = u >= 0 ? s_up[warp][u] : -1;
+        const int u = sm.up[i];
+        na[k] = sm.anc[i] | (u >= 0 ? sm.anc[u] : 0ull);
+        nd[k] = sm.dep[i] + (u >= 0 ? sm.dep[u] : 0);
+        nu[k] = u >= 0 ? sm.up[u] : -1;
       }
     }
     __syncwarp();
     for (int k = 0; k < 2; ++k) {
       const int i = lane + 32 * k;
       if (i < T) {
-        s_anc[warp][i] = na[k];
-        s_dep[warp][i] = nd[k];
-        s_up[warp][i] = nu[k];
+        sm.anc[i] = na[k];
+        sm.dep[i] = nd[k];
+        sm.up[i] = nu[k];
       }
     }
     __syncwarp();
@@ -245,11 +143,11 @@ __global__ void __launch_bounds__(kPathWarps * 32) accept_path_kernel(AcceptPara
     const int i0 = lane, i1 = lane + 32;
     if (i0 < T && i0 > 0) {
       const int p = par[i0];
-      mis0 = !(p >= 0 && p < i0) || tok[i0] != s_am[warp][p];
+      mis0 = !(p >= 0 && p < i0) || tok[i0] != sm.am[p];
     }
     if (i1 < T) {
       const int p = par[i1];
-      mis1 = !(p >= 0 && p < i1) || tok[i1] != s_am[warp][p];
+      mis1 = !(p >= 0 && p < i1) || tok[i1] != sm.am[p];
     }
   }
   const unsigned long long mis = (unsigned long long)__ballot_sync(0xffffffffu, mis0) |
@@ -259,9 +157,9 @@ __global__ void __launch_bounds__(kPathWarps * 32) accept_path_kernel(AcceptPara
   for (int k = 0; k < 2; ++k) {
     const int i = lane + 32 * k;
     if (i < T) {
-      const int d = s_dep[warp][i];
+      const int d = sm.dep[i];
       deep_ok = deep_ok && d <= a.max_depth;
-      if ((s_anc[warp][i] & mis) == 0ull) key = max(key, (d << 8) | (255 - i));
+      if ((sm.anc[i] & mis) == 0ull) key = max(key, (d << 8) | (255 - i));
     }
   }
   const bool all_ok = ok && __all_sync(0xffffffffu, deep_ok);
@@ -272,55 +170,183 @@ __global__ void __launch_bounds__(kPathWarps * 32) accept_path_kernel(AcceptPara
     if (lane == 0) {
       set_status(a.status, kStTree);
       a.accept_len[b] = 0;
-      a.next_token[b] = s_am[warp][0];
+      a.next_token[b] = sm.am[0];
+      sm.len = 0;
+      sm.path[0] = 0;
     }
     for (int d = lane; d <= a.max_depth; d += 32) path[d] = d == 0 ? 0 : -1;
+    __syncwarp();
     return;
   }
   const int end = 255 - (key & 255);
-  const unsigned long long on_path = s_anc[warp][end];
-  const int len = s_dep[warp][end];
+  const unsigned long long on_path = sm.anc[end];
+  const int len = sm.dep[end];
   for (int d = lane; d <= a.max_depth; d += 32)
     if (d > len) path[d] = -1;
   for (int k = 0; k < 2; ++k) {
     const int i = lane + 32 * k;
-    if (i < T && ((on_path >> i) & 1ull)) path[s_dep[warp][i]] = i;
+    if (i < T && ((on_path >> i) & 1ull)) {
+      path[sm.dep[i]] = i;
+      sm.path[sm.dep[i]] = i;
+    }
   }
   if (lane == 0) {
     a.accept_len[b] = len;
-    a.next_token[b] = s_am[warp][end];
+    a.next_token[b] = sm.am[end];
+    sm.len = len;
+  }
+  __syncwarp();
+}
+
+// Called by every thread of a row's CTA once thread 0 holds the row's argmax
+// ix and the prefetched sequence data is in shared memory (after a block
+// synchronisation): publish the argmax; the CTA that completes its sequence
+// selects the path and, when kCommit, commits the sequence.  The block-table
+// window for the commit is loaded before the arrival, so that its latency
+// overlaps the arrival's.
+template <bool kCommit>
+__device__ void finish_row(const AcceptParams& a, const CommitParams& c, int row, int ix, FinishSmem& sm,
+                           uint4* stage, int stage_vecs) {
+  const int b = row / a.T;
+  if (kCommit) commit_load_window(c, b, sm.seq_len, sm.commit);
+  if (threadIdx.x == 0) {
+    a.argmax_out[row] = ix;
+    __threadfence();  // the argmax is visible before the arrival is
+    sm.last = atomicAdd(&a.counters[b], 1u) == (unsigned)(a.T - 1);
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();  // every other row's argmax is visible past this point
+  if (threadIdx.x == 0) a.counters[b] = 0;  // left at zero for the next call
+  if (threadIdx.x < 32) select_path(a, b, sm);
+  if (kCommit) {
+    __syncthreads();
+    commit_sequence(c, b, sm.seq_len, sm.len, sm.path, sm.commit, stage, stage_vecs);
   }
 }
 
-template <typename T>
-cudaError_t launch_t(const AcceptParams& a, cudaStream_t stream) {
-  const int nrows = a.B * a.T;
-  if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0) {
-    argmax_scalar_kernel<T><<<nrows, kThreads, 0, stream>>>(a);
-  } else {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int grid = nrows < sms ? nrows : sms;
-    const size_t smem = (size_t)kStages * kChunkBytes;
-    cudaError_t e = cudaFuncSetAttribute(argmax_stream_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    argmax_stream_kernel<T><<<grid, kStreamThreads, smem, stream>>>(a);
+// Per-node argmax, one CTA per row, for rows of 16-byte vectors.  Each thread
+// takes the vectors tid, tid + kRowThreads, ... in increasing index order,
+// kBatch of them per round with all their loads issued before any is used
+// (streaming loads: the logits are read once), keeping (max, first index): a
+// vector's packed maximum is compared first and the vector is searched only
+// when it beats the running maximum.  Warps, then the block, merge the
+// threads' results in the same order.
+constexpr int kRowThreads = 128;
+constexpr int kBatch = 8;
+
+template <typename T, bool kCommit>
+__global__ void __launch_bounds__(kRowThreads, 8) argmax_rows_kernel(AcceptParams a, CommitParams c, int stage_vecs) {
+  constexpr int EPV = 16 / sizeof(T);
+  extern __shared__ uint4 stage[];  // the commit's row stage (kCommit)
+  __shared__ float s_v[kRowThreads / 32];
+  __shared__ int s_i[kRowThreads / 32];
+  __shared__ FinishSmem sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  SeqPrefetch pf;
+  pf.load(a, c, row / a.T, kCommit);
+  const int nvec = a.V / EPV;
+  const uint4* lg = reinterpret_cast<const uint4*>(static_cast<const T*>(a.logits) + (size_t)row * a.V);
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  for (int v0 = tid; v0 < nvec; v0 += kRowThreads * kBatch) {
+    uint4 raw[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int v = v0 + j * kRowThreads;
+      if (v < nvec) raw[j] = __ldcs(lg + v);
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int v = v0 + j * kRowThreads;
+      if (v < nvec) {
+        const float m = Max8<T>::of(raw[j]);
+        if (m > best || bidx == 0x7fffffff) {
+          T tmp[EPV];
+          memcpy(tmp, &raw[j], 16);
+#pragma unroll
+          for (int e = EPV - 1; e >= 0; --e)
+            if (Act<T>::to_f(tmp[e]) == m) bidx = v * EPV + e;
+          best = m;
+        }
+      }
+    }
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  accept_path_kernel<<<(a.B + kPathWarps - 1) / kPathWarps, kPathWarps * 32, 0, stream>>>(a);
+  warp_best(best, bidx);
+  if (lane == 0) {
+    s_v[warp] = best;
+    s_i[warp] = bidx;
+  }
+  pf.store(a, sm);
+  __syncthreads();
+  float v = lane < kRowThreads / 32 ? s_v[lane] : -INFINITY;
+  int ix = lane < kRowThreads / 32 ? s_i[lane] : 0x7fffffff;
+  warp_best(v, ix);  // every warp merges; thread 0's result is used
+  finish_row<kCommit>(a, c, row, ix, sm, stage, stage_vecs);
+}
+
+// Rows that are not 16-byte aligned: one CTA per row, scalar loads.
+template <typename T, bool kCommit>
+__global__ void __launch_bounds__(kThreads) argmax_scalar_kernel(AcceptParams a, CommitParams c, int stage_vecs) {
+  extern __shared__ uint4 stage[];  // the commit's row stage (kCommit)
+  __shared__ float s_v[kThreads / 32];
+  __shared__ int s_i[kThreads / 32];
+  __shared__ FinishSmem sm;
+  const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  SeqPrefetch pf;
+  pf.load(a, c, row / a.T, kCommit);
+  const T* lg = static_cast<const T*>(a.logits) + (size_t)row * a.V;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  for (int v = threadIdx.x; v < a.V; v += kThreads) {
+    const float x = Act<T>::to_f(lg[v]);
+    if (better(x, v, best, bidx)) { best = x; bidx = v; }
+  }
+  warp_best(best, bidx);
+  if (lane == 0) { s_v[warp] = best; s_i[warp] = bidx; }
+  pf.store(a, sm);
+  __syncthreads();
+  float v = lane < kThreads / 32 ? s_v[lane] : -INFINITY;
+  int ix = lane < kThreads / 32 ? s_i[lane] : 0x7fffffff;
+  warp_best(v, ix);
+  finish_row<kCommit>(a, c, row, ix, sm, stage, stage_vecs);
+}
+
+// The fused kernel's commit stage: every row's CTA carries it, so it stays
+// small enough for 7 CTAs per SM (the serving trees' five path entries of 8
+// bf16 heads of 128 fit in one pass).
+constexpr int kStageCap = 20 * 1024;
+
+template <typename T, bool kCommit>
+cudaError_t launch_t(const AcceptParams& a, const CommitParams& c, cudaStream_t stream) {
+  const int nrows = a.B * a.T;
+  const int sv = kCommit ? commit_stage_vecs(c, kStageCap) : 0;
+  const size_t smem = (size_t)sv * 16;
+  if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0)
+    argmax_scalar_kernel<T, kCommit><<<nrows, kThreads, smem, stream>>>(a, c, sv);
+  else
+    argmax_rows_kernel<T, kCommit><<<nrows, kRowThreads, smem, stream>>>(a, c, sv);
   return cudaGetLastError();
+}
+
+template <bool kCommit>
+cudaError_t launch_dtype(const AcceptParams& a, const CommitParams& c, int dtype, cudaStream_t stream) {
+  switch (dtype) {
+    case 0: return launch_t<float, kCommit>(a, c, stream);
+    case 1: return launch_t<__half, kCommit>(a, c, stream);
+    default: return launch_t<__nv_bfloat16, kCommit>(a, c, stream);
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_accept(const AcceptParams& a, int dtype, cudaStream_t stream) {
-  switch (dtype) {
-    case 0: return launch_t<float>(a, stream);
-    case 1: return launch_t<__half>(a, stream);
-    default: return launch_t<__nv_bfloat16>(a, stream);
-  }
+  return launch_dtype<false>(a, CommitParams{}, dtype, stream);
+}
+
+cudaError_t launch_accept_commit(const AcceptParams& a, const CommitParams& c, int dtype, cudaStream_t stream) {
+  return launch_dtype<true>(a, c, dtype, stream);
 }
 
 }  // namespace mt

@@ -316,6 +316,47 @@ int mt_kv_commit(const mt_attn_desc* d, int max_depth, const int32_t* accept_pat
   return cuda_status(launch_commit(c, stream));
 }
 
+int mt_tree_accept_commit(const mt_attn_desc* d, int vocab, int max_depth, mt_dtype logits_dtype,
+                          const int32_t* tree_tokens, const void* target_logits,
+                          const int32_t* tree_parents, int32_t* argmax_out, int32_t* accept_len,
+                          int32_t* accept_path, int32_t* next_token, void* k_cache, void* v_cache,
+                          int32_t* block_tables, int32_t* seq_lens, int32_t* released_pages,
+                          void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  int st = check_desc(d);
+  if (st != MT_OK) return st;
+  const int batch = d->batch, tree_size = d->tree_size;
+  if (batch > (1 << 24) / kMaxTree) return MT_ERR_INVALID_ARG;
+  if (vocab < 1 || max_depth < 0 || max_depth >= kMaxTree) return MT_ERR_INVALID_ARG;
+  if (logits_dtype != MT_F32 && logits_dtype != MT_F16 && logits_dtype != MT_BF16)
+    return MT_ERR_UNSUPPORTED;
+  if (!tree_tokens || !target_logits || !tree_parents || !argmax_out || !accept_len ||
+      !accept_path || !next_token || !k_cache || !v_cache || !block_tables || !seq_lens ||
+      !released_pages || !workspace)
+    return MT_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(workspace) % kAlign) ||
+      ws_bytes < mt_tree_accept_workspace_size(batch, tree_size))
+    return MT_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  AcceptParams a{};
+  a.B = batch; a.T = tree_size; a.V = vocab; a.max_depth = max_depth;
+  a.tokens = tree_tokens; a.logits = target_logits; a.parents = tree_parents;
+  a.argmax_out = argmax_out; a.accept_len = accept_len; a.accept_path = accept_path;
+  a.next_token = next_token;
+  a.status = reinterpret_cast<int*>(ws);
+  a.counters = reinterpret_cast<unsigned*>(ws + kAlign);
+  CommitParams c{};
+  c.B = batch; c.T = tree_size; c.Hkv = d->num_kv_heads; c.D = d->head_dim;
+  c.P = d->page_size; c.max_blocks = d->max_blocks_per_seq; c.num_pages = d->num_pages;
+  c.max_depth = max_depth;
+  c.rel_width = (tree_size + 2 * d->page_size - 2) / d->page_size;
+  c.elem_bytes = elem_bytes(d->dtype);
+  c.accept_path = accept_path; c.accept_len = accept_len;
+  c.k_cache = k_cache; c.v_cache = v_cache; c.block_tables = block_tables;
+  c.seq_lens = seq_lens; c.released = released_pages;
+  c.status = a.status;
+  return cuda_status(launch_accept_commit(a, c, logits_dtype, stream));
+}
+
 int mt_tree_candidates(int batch, int tree_size, int heads, int vocab, mt_dtype logits_dtype,
                        const void* root_logits, const void* head_logits,
                        const int32_t* tree_parents, int32_t* tree_tokens, void* status_ws,

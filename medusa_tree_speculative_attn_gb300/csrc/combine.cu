@@ -12,124 +12,154 @@ namespace mt {
 
 namespace {
 
-constexpr int kWarps = 8;
 constexpr int kMaxListed = 1024;  // pieces listed per pass
 
-// Block: one segment, 32 rows.  The piece list is built once per block; each
-// thread then merges one row (lane) for the 4-column groups warp, warp + 8, ...
-// (partial reads coalesced along rows), the block stages the merged rows in
-// shared memory and writes them out in 16-byte chunks along each row.
-template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(AttnParams a) {
-  constexpr int C4 = D / 4;                 // 4-column groups per row
-  constexpr int PER = C4 / kWarps;          // groups per thread
-  constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte output chunks per row
-  __shared__ int s_slot[kMaxListed];
-  __shared__ int s_count, s_single;
-  __shared__ __align__(16) T s_out[32][D + 16 / (int)sizeof(T)];
-  const Sched& s = a.sched;
-  const int seg = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int RG = a.rows_per_group;
-  const int HR = s.Hkv * s.nrg;
-  const int b = seg / HR, seg_in_b = seg % HR;
-  const int kvh = seg_in_b / s.nrg, rg = seg_in_b % s.nrg;
-  const int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
-  if (nt == 0) return;  // invalid sequence (block-uniform)
-
-  // the slots holding this segment's pieces
-  int slot0, count;
-  long long t0 = 0, W = 0;
-  if (s.splits == 0) {
-    W = sched_total_cost(s);  // balanced mode works in cost units
-    t0 = (long long)s.tile_pfx[b] * HR + (long long)seg_in_b * nt;
-    const int c0 = sched_cta_of(sched_tile_cost(s, t0, seg), W, s.G);
-    const int c1 = sched_cta_of(sched_tile_cost(s, t0 + nt - 1, seg), W, s.G);
-    if (c0 == c1) return;  // written directly by its only CTA
-    slot0 = seg + c0;
-    count = c1 - c0 + 1;
-  } else {
-    if (s.splits == 1) return;
-    slot0 = seg * s.splits;
-    count = s.splits;
-  }
-  const int row0 = blockIdx.y * 32;
-  float M = -INFINITY, lsum = 0.f;
-  float4 acc[PER];
-#pragma unroll
-  for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int r = row0 + lane;
-  const int PR = a.part_rows;
-  const bool row_ok = r < PR && rg * RG + r < a.rows;
-  for (int k0 = 0; k0 < count; k0 += kMaxListed) {
-    // list the pieces [k0, k0 + kMaxListed) that exist
-    if (tid == 0) s_count = 0;
-    __syncthreads();
-    for (int k = k0 + tid; k < count && k < k0 + kMaxListed; k += blockDim.x) {
-      bool exists;
-      if (s.splits == 0) {
-        // the segment's tiles are one contiguous stretch of the cost axis:
-        // its first and last owners hold tiles of it, and a CTA in between
-        // covers its whole cost range inside it, so it holds tiles exactly
-        // when that range is not empty
-        const int c = slot0 - seg + k;
-        exists = k == 0 || k == count - 1 || W * (c + 1) / s.G > W * c / s.G;
-      } else {
-        exists = (long long)nt * k / s.splits < (long long)nt * (k + 1) / s.splits;
-      }
-      s_slot[k - k0] = exists ? slot0 + k : -1;
-    }
-    __syncthreads();
-    const int n = min(kMaxListed, count - k0);
-    if (row_ok) {
-      for (int k = 0; k < n; ++k) {
-        const int slot = s_slot[k];
-        if (slot < 0) continue;
-        const float2 ml = a.part_ml[(size_t)slot * PR + r];
-        if (ml.x == -INFINITY) continue;  // the piece saw no key of this row
-        const float m_new = fmaxf(M, ml.x);
-        const float c_old = exp2f(M - m_new), c_new = exp2f(ml.x - m_new);
-        lsum = lsum * c_old + ml.y * c_new;
-#pragma unroll
-        for (int e = 0; e < PER; ++e) {
-          const float4 v = a.part_o[((size_t)slot * C4 + warp + kWarps * e) * PR + r];
-          acc[e].x = acc[e].x * c_old + v.x * c_new;
-          acc[e].y = acc[e].y * c_old + v.y * c_new;
-          acc[e].z = acc[e].z * c_old + v.z * c_new;
-          acc[e].w = acc[e].w * c_old + v.w * c_new;
-        }
-        M = m_new;
-      }
-    }
-    __syncthreads();
-  }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+// Fold one piece (max ml.x, sum ml.y, unnormalised columns v) into the running
+// result; a piece that saw no key of the row (ml.x = -inf) is skipped.
+template <int PER>
+__device__ __forceinline__ void merge(float& M, float& lsum, float4 (&acc)[PER], float2 ml, const float4 (&v)[PER]) {
+  if (ml.x == -INFINITY) return;
+  const float m_new = fmaxf(M, ml.x);
+  const float c_old = exp2f(M - m_new), c_new = exp2f(ml.x - m_new);
+  lsum = lsum * c_old + ml.y * c_new;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    const int c = 4 * (warp + kWarps * e);
-    s_out[lane][c] = Act<T>::from_f(acc[e].x * inv);
-    s_out[lane][c + 1] = Act<T>::from_f(acc[e].y * inv);
-    s_out[lane][c + 2] = Act<T>::from_f(acc[e].z * inv);
-    s_out[lane][c + 3] = Act<T>::from_f(acc[e].w * inv);
+    acc[e].x = acc[e].x * c_old + v[e].x * c_new;
+    acc[e].y = acc[e].y * c_old + v[e].y * c_new;
+    acc[e].z = acc[e].z * c_old + v[e].z * c_new;
+    acc[e].w = acc[e].w * c_old + v[e].w * c_new;
   }
-  __syncthreads();
-  // 32 rows x CH chunks, consecutive threads along a row
-  for (int idx = tid; idx < 32 * CH; idx += blockDim.x) {
-    const int lr = idx / CH, ch = idx % CH;
-    const int rr = row0 + lr;
-    const int row = rg * RG + rr;
-    if (rr >= PR || row >= a.rows) continue;
-    const int node = row / a.g, h = kvh * a.g + row % a.g;
-    T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
-    reinterpret_cast<uint4*>(dst)[ch] = *reinterpret_cast<const uint4*>(&s_out[lr][ch * (16 / sizeof(T))]);
+  M = m_new;
+}
+
+constexpr int kWarps = 8;
+constexpr int kBlocksPerSm = 2;
+constexpr int kRound = 4;          // pieces whose loads are in flight together
+constexpr int kPfxCached = 2048;  // tile prefixes copied to shared memory up to this batch
+
+// Persistent blocks over the items (segment, 32-row block), the tile prefix
+// copied to shared memory once, so that an item whose segment was written
+// directly is skipped without a memory access.  For an item, the block lists
+// the segment's pieces; thread (warp w, lane l) merges row l for the 4-column
+// groups w, w + 8, ... (partial reads coalesced along rows), kRound pieces per
+// round with all their loads in flight; the block stages the merged rows in
+// shared memory and writes them out in 16-byte chunks along each row.
+template <typename T, int D>
+__global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(AttnParams a) {
+  constexpr int C4 = D / 4;                    // 4-column groups per row
+  constexpr int PER = C4 / kWarps;             // groups per thread
+  constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte output chunks per row
+  __shared__ int s_pfx[kPfxCached + 1];
+  __shared__ int s_slot[kMaxListed];
+  __shared__ __align__(16) T s_out[32][D + 16 / (int)sizeof(T)];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  Sched s = a.sched;
+  if (s.B <= kPfxCached) {
+    for (int i = tid; i <= s.B; i += blockDim.x) s_pfx[i] = s.tile_pfx[i];
+    __syncthreads();
+    s.tile_pfx = s_pfx;
+  }
+  const int RG = a.rows_per_group;
+  const int HR = s.Hkv * s.nrg;
+  const int PR = a.part_rows;
+  const int nrb = (PR + 31) / 32;
+  const long long items = (long long)s.B * HR * nrb;
+  const long long W = s.splits == 0 ? sched_total_cost(s) : 0;  // balanced mode works in cost units
+  for (long long item = blockIdx.x; item < items; item += gridDim.x) {
+    const int seg = (int)(item / nrb), row0 = (int)(item % nrb) * 32;
+    const int b = seg / HR, seg_in_b = seg % HR;
+    const int kvh = seg_in_b / s.nrg, rg = seg_in_b % s.nrg;
+    const int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
+    if (nt == 0) continue;  // invalid sequence (block-uniform)
+    // the slots holding this segment's pieces
+    int slot0, count;
+    if (s.splits == 0) {
+      const long long t0 = (long long)s.tile_pfx[b] * HR + (long long)seg_in_b * nt;
+      const int c0 = sched_cta_of(sched_tile_cost(s, t0, seg), W, s.G);
+      const int c1 = sched_cta_of(sched_tile_cost(s, t0 + nt - 1, seg), W, s.G);
+      if (c0 == c1) continue;  // written directly by its only CTA
+      slot0 = seg + c0;
+      count = c1 - c0 + 1;
+    } else {
+      if (s.splits == 1) continue;
+      slot0 = seg * s.splits;
+      count = s.splits;
+    }
+    float M = -INFINITY, lsum = 0.f;
+    float4 acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int r = row0 + lane;
+    const bool row_ok = r < PR && rg * RG + r < a.rows;
+    for (int k0 = 0; k0 < count; k0 += kMaxListed) {
+      // list the pieces [k0, k0 + kMaxListed) that exist
+      __syncthreads();  // the previous list is no longer read
+      for (int k = k0 + tid; k < count && k < k0 + kMaxListed; k += blockDim.x) {
+        bool exists;
+        if (s.splits == 0) {
+          // the segment's tiles are one contiguous stretch of the cost axis:
+          // its first and last owners hold tiles of it, and a CTA in between
+          // covers its whole cost range inside it, so it holds tiles exactly
+          // when that range is not empty
+          const int c = slot0 - seg + k;
+          exists = k == 0 || k == count - 1 || W * (c + 1) / s.G > W * c / s.G;
+        } else {
+          exists = (long long)nt * k / s.splits < (long long)nt * (k + 1) / s.splits;
+        }
+        s_slot[k - k0] = exists ? slot0 + k : -1;
+      }
+      __syncthreads();
+      const int n = min(kMaxListed, count - k0);
+      if (row_ok) {
+        for (int k = 0; k < n; k += kRound) {
+          float2 ml[kRound];
+          float4 v[kRound][PER];
+#pragma unroll
+          for (int j = 0; j < kRound; ++j) {
+            const int slot = k + j < n ? s_slot[k + j] : -1;
+            ml[j] = make_float2(-INFINITY, 0.f);
+            if (slot >= 0) {
+              ml[j] = a.part_ml[(size_t)slot * PR + r];
+#pragma unroll
+              for (int e = 0; e < PER; ++e) v[j][e] = a.part_o[((size_t)slot * C4 + warp + kWarps * e) * PR + r];
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kRound; ++j) merge<PER>(M, lsum, acc, ml[j], v[j]);
+        }
+      }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) {
+      const int c = 4 * (warp + kWarps * e);
+      s_out[lane][c] = Act<T>::from_f(acc[e].x * inv);
+      s_out[lane][c + 1] = Act<T>::from_f(acc[e].y * inv);
+      s_out[lane][c + 2] = Act<T>::from_f(acc[e].z * inv);
+      s_out[lane][c + 3] = Act<T>::from_f(acc[e].w * inv);
+    }
+    __syncthreads();
+    // 32 rows x CH chunks, consecutive threads along a row
+    for (int idx = tid; idx < 32 * CH; idx += blockDim.x) {
+      const int lr = idx / CH, ch = idx % CH;
+      const int rr = row0 + lr;
+      const int row = rg * RG + rr;
+      if (rr >= PR || row >= a.rows) continue;
+      const int node = row / a.g, h = kvh * a.g + row % a.g;
+      T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
+      reinterpret_cast<uint4*>(dst)[ch] = *reinterpret_cast<const uint4*>(&s_out[lr][ch * (16 / sizeof(T))]);
+    }
+    __syncthreads();  // s_out is rewritten by the next item
   }
 }
 
 template <typename T, int D>
 cudaError_t launch_t(const AttnParams& a, cudaStream_t stream) {
-  const int nseg = a.B * a.Hkv * a.sched.nrg;
-  dim3 grid(nseg, (a.part_rows + 31) / 32);
-  combine_kernel<T, D><<<grid, kWarps * 32, 0, stream>>>(a);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long items = (long long)a.B * a.Hkv * a.sched.nrg * ((a.part_rows + 31) / 32);
+  const long long grid = items < (long long)kBlocksPerSm * sms ? items : (long long)kBlocksPerSm * sms;
+  combine_kernel<T, D><<<(unsigned)(grid > 0 ? grid : 1), kWarps * 32, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -52,7 +52,6 @@ struct AcceptParams {
 
 struct CommitParams {
   int B, T, Hkv, D, P, max_blocks, num_pages, max_depth, rel_width, elem_bytes;
-  int stage_vecs;  // 16-byte entries of the shared staging buffer
   const int* accept_path;
   const int* accept_len;
   void* k_cache;
@@ -83,6 +82,8 @@ cudaError_t launch_attn_tc(const AttnParams& a, int dtype, const void* tmap_k, c
 cudaError_t launch_combine(const AttnParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_cand(const CandParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_accept(const AcceptParams& a, int dtype, cudaStream_t stream);
+// Acceptance and, per sequence as soon as its path is known, the KV commit.
+cudaError_t launch_accept_commit(const AcceptParams& a, const CommitParams& c, int dtype, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& a, cudaStream_t stream);
 
 }  // namespace mt

@@ -82,69 +82,121 @@ __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
   return total;
 }
 
+// Sequences whose trees block 0 checks per round (their parents and depths
+// staged in shared memory, every load of a round issued together).
+constexpr int kSchedSeqs = 16;
+
+// Ancestor masks of sequence b by one warp.  Lane l owns nodes l and l + 32;
+// the sets come from pointer jumping in shared memory: start from {i} and the
+// parent link, then six rounds of  anc[i] |= anc[up[i]], up[i] = up[up[i]]
+// close them for any depth < 64.  An invalid tree or prefix length writes 0
+// masks (the attention kernels skip such sequences).
+__device__ void ancestor_masks(const PrepParams& a, int b, unsigned long long* s_anc, int* s_up) {
+  const int lane = threadIdx.x & 31;
+  const int* par = a.tree_parents + (size_t)b * a.T;
+  const int* dep = a.tree_depths + (size_t)b * a.T;
+  const int L = a.seq_lens[b];
+  bool good = true;
+  for (int i = lane; i < a.T; i += 32) {
+    const int p = par[i];
+    const bool ok_i = i == 0 ? (p == -1 && dep[0] == 0) : (p >= 0 && p < i && dep[i] == dep[p] + 1);
+    good = good && ok_i;
+    s_anc[i] = 1ull << i;
+    s_up[i] = ok_i ? p : -1;
+  }
+  const bool ok = __all_sync(0xffffffffu, good);
+  __syncwarp();
+  for (int round = 0; round < 6; ++round) {
+    unsigned long long na[2];
+    int nu[2];
+    for (int k = 0; k < 2; ++k) {
+      const int i = lane + 32 * k;
+      if (i < a.T) {
+        const int u = s_up[i];
+        na[k] = s_anc[i] | (u >= 0 ? s_anc[u] : 0ull);
+        nu[k] = u >= 0 ? s_up[u] : -1;
+      }
+    }
+    __syncwarp();
+    for (int k = 0; k < 2; ++k) {
+      const int i = lane + 32 * k;
+      if (i < a.T) {
+        s_anc[i] = na[k];
+        s_up[i] = nu[k];
+      }
+    }
+    __syncwarp();
+  }
+  const bool len_ok = L >= 0 && (long long)L + a.T <= (long long)a.max_blocks * a.P;
+  for (int i = lane; i < a.T; i += 32)
+    a.anc[(size_t)b * a.T + i] = (ok && len_ok) ? s_anc[i] : 0ull;  // 0 marks invalid
+  __syncwarp();
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
   const int tid = threadIdx.x;
   if (blockIdx.x == 0) {
-    // ---- schedule block (block 0: dispatched first): validate trees, ancestor masks, tile prefix ----
-    // One warp per sequence; lane l owns nodes l and l + 32.  Ancestor sets by
-    // pointer jumping in shared memory: start from {i} and the parent link,
-    // then six rounds of  anc[i] |= anc[up[i]], up[i] = up[up[i]]  close them
-    // for any depth < 64.
+    // ---- schedule block (block 0: dispatched first): tree and length
+    // checks, tiles per segment, their prefix, and the CTAs' piece lists.
+    // The same checks as ancestor_masks: a parent earlier than its child and
+    // depth[i] = depth[parent[i]] + 1 (the root at depth 0 with parent -1).
     extern __shared__ int s_nt[];  // [B + 1] tiles per segment, then [B] prefix lengths
     int* s_len = s_nt + a.B + 1;
     __shared__ int s_warp[32];
-    __shared__ unsigned long long s_anc[kPrepThreads / 32][kMaxTree];
-    __shared__ int s_up[kPrepThreads / 32][kMaxTree];
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int b = warp; b < a.B; b += kPrepThreads / 32) {
-      const int* par = a.tree_parents + (size_t)b * a.T;
-      const int* dep = a.tree_depths + (size_t)b * a.T;
-      bool good = true;
-      for (int i = lane; i < a.T; i += 32) {
-        const int p = par[i];
-        const bool ok_i = i == 0 ? (p == -1 && dep[0] == 0)
-                                 : (p >= 0 && p < i && dep[i] == dep[p] + 1);
-        good = good && ok_i;
-        s_anc[warp][i] = 1ull << i;
-        s_up[warp][i] = ok_i ? p : -1;
-      }
-      const bool ok = __all_sync(0xffffffffu, good);
-      __syncwarp();
-      for (int round = 0; round < 6; ++round) {
-        unsigned long long na[2];
-        int nu[2];
-        for (int k = 0; k < 2; ++k) {
-          const int i = lane + 32 * k;
-          if (i < a.T) {
-            const int u = s_up[warp][i];
-            na[k] = s_anc[warp][i] | (u >= 0 ? s_anc[warp][u] : 0ull);
-            nu[k] = u >= 0 ? s_up[warp][u] : -1;
-          }
+    __shared__ int s_par[kSchedSeqs * kMaxTree], s_dep[kSchedSeqs * kMaxTree];
+    __shared__ int s_ok[kSchedSeqs];
+    constexpr int kPer = kSchedSeqs * kMaxTree / kPrepThreads;
+    for (int b0 = 0; b0 < a.B; b0 += kSchedSeqs) {
+      const int nb = min(kSchedSeqs, a.B - b0);
+      const int n = nb * a.T;
+      const int* par = a.tree_parents + (size_t)b0 * a.T;
+      const int* dep = a.tree_depths + (size_t)b0 * a.T;
+      int pv[kPer], dv[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int e = tid + k * kPrepThreads;
+        if (e < n) {
+          pv[k] = par[e];
+          dv[k] = dep[e];
         }
-        __syncwarp();
-        for (int k = 0; k < 2; ++k) {
-          const int i = lane + 32 * k;
-          if (i < a.T) {
-            s_anc[warp][i] = na[k];
-            s_up[warp][i] = nu[k];
-          }
-        }
-        __syncwarp();
       }
-      const int L = a.seq_lens[b];
-      const bool len_ok = L >= 0 && (long long)L + a.T <= (long long)a.max_blocks * a.P;
-      if (lane == 0) s_len[b] = L;
-      for (int i = lane; i < a.T; i += 32)
-        a.anc[(size_t)b * a.T + i] = (ok && len_ok) ? s_anc[warp][i] : 0ull;  // 0 marks invalid
-      if (lane == 0) {
+      if (tid < nb) {
+        s_len[b0 + tid] = a.seq_lens[b0 + tid];
+        s_ok[tid] = 1;
+      }
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int e = tid + k * kPrepThreads;
+        if (e < n) {
+          s_par[e] = pv[k];
+          s_dep[e] = dv[k];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int e = tid + k * kPrepThreads;
+        if (e < n) {
+          const int sb = e / a.T, i = e % a.T;
+          const int p = s_par[e];
+          const bool ok_i = i == 0 ? (p == -1 && s_dep[e] == 0)
+                                   : (p >= 0 && p < i && s_dep[e] == s_dep[sb * a.T + p] + 1);
+          if (!ok_i) s_ok[sb] = 0;
+        }
+      }
+      __syncthreads();
+      if (tid < nb) {
+        const int b = b0 + tid;
+        const int L = s_len[b];
+        const bool ok = s_ok[tid] != 0;
+        const bool len_ok = L >= 0 && (long long)L + a.T <= (long long)a.max_blocks * a.P;
         if (!ok) set_status(a.status, kStTree);
         if (!len_ok) set_status(a.status, kStPages);
         s_nt[b] = (ok && len_ok) ? (L + a.T + kTileKeys - 1) / kTileKeys : 0;
       }
-      __syncwarp();
+      __syncthreads();
     }
-    __syncthreads();
     int total = block_exclusive_scan(s_nt, a.B, s_warp);
     for (int b = tid; b < a.B; b += blockDim.x) a.tile_pfx[b] = s_nt[b];
     if (tid == 0) {
@@ -179,19 +231,26 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
     }
     return;
   }
+  // ---- ancestor masks: one warp per sequence, before its rotation rows ----
+  const long long nwarps = (long long)(gridDim.x - 1) * (kPrepThreads / 32);
+  const long long gwarp = (long long)(blockIdx.x - 1) * (kPrepThreads / 32) + (tid >> 5);
+  {
+    __shared__ unsigned long long s_anc[kPrepThreads / 32][kMaxTree];
+    __shared__ int s_up[kPrepThreads / 32][kMaxTree];
+    for (long long b = gwarp; b < a.B; b += nwarps) ancestor_masks(a, (int)b, s_anc[tid >> 5], s_up[tid >> 5]);
+  }
   // ---- rotations: B*T*Hq query rows, then B*T*Hkv key/value rows ----
   // A row is handled by D/16 lanes; lane k rotates the pairs (j, j + D/2) for
-  // j in [8k, 8k + 8) with 16-byte (8-element) loads and stores.
+  // j in [8k, 8k + 8) with 16-byte (8-element) loads and stores.  The row's
+  // own data is loaded before the prefix length and depth it is placed by.
   const int lanes_per_row = a.D / 16;
   const int rows_per_warp = 32 / lanes_per_row;
   const int lane = tid & 31;
   const int sub = lane / lanes_per_row, k = lane % lanes_per_row;
   const long long nq = (long long)a.B * a.T * a.Hq;
   const long long nk = (long long)a.B * a.T * a.Hkv;
-  const long long nwarps = (long long)(gridDim.x - 1) * (kPrepThreads / 32);
   const int half = a.D / 2;
-  for (long long row0 = ((long long)(blockIdx.x - 1) * (kPrepThreads / 32) + (tid >> 5)) * rows_per_warp;
-       row0 < nq + nk; row0 += nwarps * rows_per_warp) {
+  for (long long row0 = gwarp * rows_per_warp; row0 < nq + nk; row0 += nwarps * rows_per_warp) {
     long long row = row0 + sub;
     if (row >= nq + nk) continue;
     const bool is_q = row < nq;
@@ -199,6 +258,15 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
     const int H = is_q ? a.Hq : a.Hkv;
     const int i = (int)((row / H) % a.T);
     const int b = (int)(row / ((long long)H * a.T));
+    const T* src = static_cast<const T*>(is_q ? a.q : a.k_new) + (size_t)row * a.D;
+    const typename Vec8<T>::type lo_raw = Vec8<T>::load(src + 8 * k);
+    const typename Vec8<T>::type hi_raw = Vec8<T>::load(src + half + 8 * k);
+    typename Vec8<T>::type vlo, vhi;
+    if (!is_q) {
+      const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
+      vlo = Vec8<T>::load(vn + 8 * k);
+      vhi = Vec8<T>::load(vn + half + 8 * k);
+    }
     const int L = a.seq_lens[b];
     const int depth = a.tree_depths[(size_t)b * a.T + i];
     const long long pos = (long long)L + depth;
@@ -206,10 +274,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
       if (k == 0) set_status(a.status, L < 0 ? kStPages : kStTree);
       continue;
     }
-    const T* src;
     T* dst;
     if (is_q) {
-      src = static_cast<const T*>(a.q) + (size_t)row * a.D;
       dst = static_cast<T*>(a.q_rot) + (size_t)row * a.D;
     } else {
       const int kvh = (int)(row % a.Hkv);
@@ -220,16 +286,12 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
         continue;
       }
       const size_t off = (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * a.D;
-      src = static_cast<const T*>(a.k_new) + (size_t)row * a.D;
       dst = static_cast<T*>(a.k_cache) + off;
       // raw value: this lane's two 8-element chunks
-      const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
       T* vc = static_cast<T*>(a.v_cache) + off;
-      Vec8<T>::store(vc + 8 * k, Vec8<T>::load(vn + 8 * k));
-      Vec8<T>::store(vc + half + 8 * k, Vec8<T>::load(vn + half + 8 * k));
+      Vec8<T>::store(vc + 8 * k, vlo);
+      Vec8<T>::store(vc + half + 8 * k, vhi);
     }
-    const typename Vec8<T>::type lo_raw = Vec8<T>::load(src + 8 * k);
-    const typename Vec8<T>::type hi_raw = Vec8<T>::load(src + half + 8 * k);
     const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * half + 8 * k);
     T lo[8], hi[8], olo[8], ohi[8];
     memcpy(lo, &lo_raw, sizeof(lo));

@@ -91,6 +91,12 @@ class Step:
         mt.kv_commit(self.path, self.alen, d["k_cache"], d["v_cache"], d["block_tables"],
                      d["seq_lens"], self.rel, tree_size=self.w["T"], status_ws=self.ws)
 
+    def accept_commit(self):
+        d = self.d
+        mt.tree_accept_commit(d["tree_tokens"], d["logits"], d["tree_parents"], self.alen, self.path,
+                              d["k_cache"], d["v_cache"], d["block_tables"], d["seq_lens"], self.rel,
+                              argmax_out=self.am, next_token=self.nxt, workspace=self.aws)
+
     def status(self):
         return mt.read_status(self.ws), mt.read_status(self.aws)
 

@@ -29,6 +29,7 @@ def declared_functions():
 def test_header_declares_the_three_calls():
     names = declared_functions()
     for n in ("mt_tree_attn_paged", "mt_tree_accept_greedy", "mt_kv_commit", "mt_tree_candidates",
+              "mt_tree_accept_commit",
               "mt_tree_attn_workspace_size", "mt_tree_accept_workspace_size", "mt_rope_create",
               "mt_rope_destroy", "mt_read_status", "mt_status_string", "mt_version"):
         assert n in names
@@ -99,6 +100,26 @@ def test_accept_and_commit_reject_bad_sizes(lib):
     assert lib.mt_kv_commit(ctypes.byref(d), 3, p, p, p, p, p, p, p, p, None) == -2
     d = _desc()
     assert lib.mt_kv_commit(ctypes.byref(d), 3, None, p, p, p, p, p, p, p, None) == -1
+
+
+def test_fused_accept_commit_rejects_bad_arguments(lib):
+    P = ctypes.c_void_p
+    buf = (ctypes.c_char * 4096)()
+    p = ctypes.cast(buf, P)
+    f = lib.mt_tree_accept_commit
+    f.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int] + [P] * 12 + [P, ctypes.c_size_t, P]
+    d = _desc()
+    ok = [p] * 12
+    assert f(ctypes.byref(_desc(tree_size=70)), 10, 3, 0, *ok, p, 4096, None) == -2  # tree too large
+    assert f(ctypes.byref(d), 0, 3, 0, *ok, p, 4096, None) == -1  # empty vocab
+    assert f(ctypes.byref(d), 10, 64, 0, *ok, p, 4096, None) == -1  # max_depth past one mask
+    assert f(ctypes.byref(d), 10, 3, 9, *ok, p, 4096, None) == -2  # unknown logits dtype
+    assert f(ctypes.byref(d), 10, 3, 0, *ok, p, 0, None) == -1  # workspace too small
+    for k in range(12):
+        args = list(ok)
+        args[k] = None
+        assert f(ctypes.byref(d), 10, 3, 0, *args, p, 4096, None) == -1  # null pointer
+    assert f(ctypes.byref(d), 10, 3, 0, *ok, None, 4096, None) == -1
 
 
 def test_candidates_reject_bad_arguments(lib):

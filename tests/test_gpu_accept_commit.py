@@ -176,3 +176,102 @@ def test_bad_tree_sets_status_without_fault():
     step = Step(w)
     step.attn()
     assert step.status()[0] == -3
+
+
+# ---- acceptance and commit in one launch (mt_tree_accept_commit) ----
+
+def _fused_check(w, step, kc0, vc0):
+    o_am = oracle.accept_greedy(w["tree_tokens"], w["logits"], w["logits_dtype"], w["tree_parents"],
+                                w["max_depth"])[0]
+    assert np.array_equal(step.am.cpu().numpy(), o_am)
+    _commit_check(w, step, kc0, vc0)
+
+
+@pytest.mark.parametrize("name", ["tiny_tree_fp32", "llama7b_b1_fp16", "serve_b16_gqa_bf16",
+                                  "verify_b64_fp16"])
+def test_fused_step_matches_oracle(name):
+    w = workloads.generate(name, seed=4)
+    step = Step(w)
+    step.attn()
+    step.accept_commit()
+    assert step.status() == (0, 0)
+    _, k_rot = oracle.rotate_inputs(w)
+    kc0, vc0 = oracle.tree_scatter(w, w["k_cache"], w["v_cache"], k_rot=k_rot)
+    _fused_check(w, step, kc0, vc0)
+    o_next = oracle.accept_greedy(w["tree_tokens"], w["logits"], w["logits_dtype"], w["tree_parents"],
+                                  w["max_depth"])[3]
+    assert np.array_equal(step.nxt.cpu().numpy(), o_next)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_fused_random_paths(dtype):
+    # long planted paths (many register passes of the commit), prefixes straddling pages
+    for seed, tree in enumerate([("chain", 20), ("fanout", (2, 2, 2, 2, 2), 40), ("star", 9),
+                                 ("chain", 64)]):
+        md = tree[1] - 1 if tree[0] == "chain" else {"fanout": 5, "star": 1}[tree[0]]
+        spec = workloads.custom("fused", B=5, Hq=8, Hkv=4, head_dim=128, dtype=dtype,
+                                prefix=("list", [0, 15, 16, 17, 300]), tree=tree, max_depth=md,
+                                vocab=50, logits_dtype="f32", plant=("uniform", 0, md))
+        w = workloads.generate(spec, seed=seed)
+        step = Step(w)
+        step.attn()
+        step.accept_commit()
+        assert step.status() == (0, 0)
+        _, k_rot = oracle.rotate_inputs(w)
+        kc0, vc0 = oracle.tree_scatter(w, w["k_cache"], w["v_cache"], k_rot=k_rot)
+        _fused_check(w, step, kc0, vc0)
+
+
+def test_fused_equals_the_two_calls_and_leaves_counters_at_zero():
+    w = workloads.generate("serve_b16_gqa_bf16", seed=6)
+    a, b = Step(w), Step(w)
+    a.attn()
+    b.attn()
+    a.accept()
+    a.commit()
+    b.accept_commit()
+    assert a.status() == (0, 0) and b.status() == (0, 0)
+    for x, y in ((a.am, b.am), (a.alen, b.alen), (a.path, b.path), (a.nxt, b.nxt), (a.rel, b.rel)):
+        assert torch.equal(x, y)
+    for key in ("block_tables", "seq_lens", "k_cache", "v_cache"):  # bytes: the pool may hold NaNs
+        assert torch.equal(a.d[key].view(torch.uint8), b.d[key].view(torch.uint8))
+    # the arrival counters are back at zero: acceptance alone on the same
+    # workspace gives the same path
+    path0 = b.path.clone()
+    b.accept()
+    assert mt.read_status(b.aws) == 0 and torch.equal(b.path, path0)
+
+
+def test_fused_bad_page_sets_status_without_fault():
+    spec = workloads.custom("fusedpage", B=3, Hq=4, Hkv=2, head_dim=128, dtype="bf16",
+                            prefix=("list", [100, 40, 7]), tree=("fanout", (3, 2), 6), max_depth=2,
+                            vocab=64, logits_dtype="bf16", plant=("uniform", 0, 2))
+    w = workloads.generate(spec, seed=1)
+    step = Step(w)
+    step.attn()
+    bt = step.d["block_tables"]
+    L1 = int(w["seq_lens"][1])
+    bt[1, (L1 + 5) // w["page_size"]] = w["num_pages"] + 5   # a scratch slot of sequence 1
+    step.accept_commit()
+    assert mt.read_status(step.aws) == mt.MedusaTreeError(-4, "").status
+    # sequence 1 is untouched; the others are committed as the oracle says
+    sl = step.d["seq_lens"].cpu().numpy()
+    assert sl[1] == L1
+    o_len = oracle.accept_greedy(w["tree_tokens"], w["logits"], w["logits_dtype"], w["tree_parents"],
+                                 w["max_depth"])[1]
+    for b in (0, 2):
+        assert sl[b] == int(w["seq_lens"][b]) + int(o_len[b]) + 1
+
+
+def test_fused_bad_tree_commits_the_root_only():
+    spec = workloads.custom("fusedtree", B=2, Hq=4, Hkv=2, head_dim=64, dtype="f16",
+                            prefix=("list", [10, 40]), tree=("fanout", (3, 2), 6), max_depth=2,
+                            vocab=64, logits_dtype="f16", plant=("uniform", 0, 2))
+    w = workloads.generate(spec, seed=0)
+    step = Step(w)
+    step.attn()
+    step.d["tree_parents"][1, 3] = 5   # parent after child: acceptance rejects the tree
+    step.accept_commit()
+    assert mt.read_status(step.aws) == -3
+    assert step.alen.cpu().numpy()[1] == 0
+    assert step.d["seq_lens"].cpu().numpy()[1] == int(w["seq_lens"][1]) + 1
