@@ -139,11 +139,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def kernel_code_fingerprint() -> str:
+    """sha256 (16 hex digits) of the tensor-core attention kernel's sources
+    with comments and blank lines removed: a comment edit keeps it, any code
+    change alters it."""
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "medusa_tree_speculative_attn_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("attn_tc.cu", "tc_ptx.cuh", "common.cuh"):
+        with open(os.path.join(csrc, f)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        for line in text.splitlines():
+            code = re.sub(r"//.*", "", line).rstrip()
+            if code.strip():
+                h.update(code.encode() + b"\n")
+    return h.hexdigest()[:16]
+
+
 def ncu_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the tensor-core attention kernel from the
     committed ncu summary, or None when that capture does not describe the
-    kernel as it is now (different workload, kernel or source)."""
-    import hashlib
+    kernel as it is now (different workload, kernel or code)."""
     path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}.md")
     if kernel == "simt" or not os.path.exists(path):
         return None
@@ -152,12 +169,7 @@ def ncu_traffic(workload: str, kernel: str):
         if ":" in line and not line.startswith(("|", "#", "`")):
             k, _, v = line.partition(":")
             fields[k.strip()] = v.strip()
-    csrc = os.path.join(ROOT, "medusa_tree_speculative_attn_gb300", "csrc")
-    h = hashlib.sha256()
-    for f in ("attn_tc.cu", "tc_ptx.cuh", "common.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
-    if fields.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+    if fields.get("kernel_code_sha256_16") != kernel_code_fingerprint():
         return None
     try:
         return int(fields["traffic_bytes_per_launch"])

@@ -18,18 +18,22 @@
 //              keep HBM busy with 2 KB boxes; four can.  Producer 0 also loads
 //              each piece's rotated queries (one 128-row x 64-col box per M
 //              tile and half);
-//   QK issuer  one thread issues S = Q K^T (M 128, N 64, K D) into TMEM;
-//   PV issuer  one thread issues O += P V (M 128, N D, K 64), P read from
-//              TMEM; separate from the QK issuer so that neither waits behind
-//              the other's dependencies;
+//   QK issuer  one thread copies each piece's queries from shared memory into
+//              TMEM and issues S = Q K^T (M 128, N 64, K D; A = Q from TMEM)
+//              into TMEM, for M tile m as soon as the softmax has read S_m;
+//   PV issuer  one thread issues O += P V (M 128, N D, K 64), P and V from
+//              shared memory; separate from the QK issuer so that neither
+//              waits behind the other's dependencies;
 //   softmax    one thread per query row: S from TMEM, tree/prefix mask (only
 //              on tiles that reach past the prefix), online softmax in base 2
 //              with a lazy rescale (O in TMEM is rescaled only when the
-//              running max grows by more than 8), P written back over S as
-//              packed 16-bit pairs; at the end of a piece O / l goes to the
-//              output (whole segment) or O, m, l to a partial slot.
-// Shared memory holds Q (up to 64 KB) and a ring of 32 KB K/V stages; TMEM
-// holds O (2 x 128 columns) and two S/P buffers per M tile (4 x 64 columns).
+//              running max grows by more than 8), P written as 16-bit values
+//              to a 128-byte-swizzled shared-memory tile; at the end of a
+//              piece O / l goes to the output (whole segment) or O, m, l to a
+//              partial slot.
+// Shared memory holds Q staging (up to 64 KB), P (16 KB per M tile) and a
+// ring of 32 KB K/V stages; TMEM holds O (2 x 128 columns), S (2 x 64) and Q
+// (2 x 64 packed 16-bit pairs).
 // Every mbarrier wait is bounded (2 s); on a timeout the kernel records
 // MT_ERR_TIMEOUT, lets the other roles bail out, waits for its own TMA loads
 // and MMAs, frees TMEM and returns.
