@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kRowThreads, 8) argmax_rows_kernel(AcceptParam
   __shared__ FinishSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x;
+  pdl_wait();
   SeqPrefetch pf;
   pf.load(a, c, row / a.T, kCommit);
   const int nvec = a.V / EPV;
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(kThreads) argmax_scalar_kernel(AcceptParams a,
   __shared__ int s_i[kThreads / 32];
   __shared__ FinishSmem sm;
   const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_wait();
   SeqPrefetch pf;
   pf.load(a, c, row / a.T, kCommit);
   const T* lg = static_cast<const T*>(a.logits) + (size_t)row * a.V;
@@ -324,10 +326,8 @@ cudaError_t launch_t(const AcceptParams& a, const CommitParams& c, cudaStream_t 
   const int sv = kCommit ? commit_stage_vecs(c, kStageCap) : 0;
   const size_t smem = (size_t)sv * 16;
   if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0)
-    argmax_scalar_kernel<T, kCommit><<<nrows, kThreads, smem, stream>>>(a, c, sv);
-  else
-    argmax_rows_kernel<T, kCommit><<<nrows, kRowThreads, smem, stream>>>(a, c, sv);
-  return cudaGetLastError();
+    return launch_pdl(argmax_scalar_kernel<T, kCommit>, dim3(nrows), dim3(kThreads), smem, stream, a, c, sv);
+  return launch_pdl(argmax_rows_kernel<T, kCommit>, dim3(nrows), dim3(kRowThreads), smem, stream, a, c, sv);
 }
 
 template <bool kCommit>

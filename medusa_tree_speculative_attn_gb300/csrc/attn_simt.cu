@@ -58,6 +58,7 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
   float* KV = Qs + R * LD;        // [64][LD]
   float* Ps = KV + kTileKeys * LD;  // [R][PLD]
   __shared__ unsigned long long s_anc[R];
+  pdl_wait();
 
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const T* __restrict__ q = static_cast<const T*>(a.q_rot);
@@ -200,8 +201,7 @@ cudaError_t launch_simt_t(const AttnParams& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  attn_simt_kernel<T, D><<<a.sched.G, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_simt_kernel<T, D>, dim3(a.sched.G), dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace

@@ -191,6 +191,14 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     tc::tmem_alloc(tmem_slot, C::kTmemCols);
     tc::tmem_relinquish();
   }
+  if (warp == C::kProducer0 && lane == 0) {
+    tc::prefetch_tmap(&tmap_k);
+    tc::prefetch_tmap(&tmap_v);
+    tc::prefetch_tmap(&tmap_q);
+  }
+  // everything above overlaps the end of the preceding kernel; the piece
+  // table, queries, masks and block tables are read only past this wait
+  pdl_wait();
   if (warp == C::kPvWarp) {
     // this CTA's piece list (written by the prep kernel) into shared memory
     const int n = a.piece_table[blockIdx.x];
@@ -198,11 +206,6 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     const int* src = a.piece_table + a.sched.G + (size_t)blockIdx.x * kMaxPieceRecs * 8;
     int* dst = reinterpret_cast<int*>(s_pieces);
     for (int e = lane; e < (n > 0 ? n : 0) * 8; e += 32) dst[e] = src[e];
-  }
-  if (warp == C::kProducer0 && lane == 0) {
-    tc::prefetch_tmap(&tmap_k);
-    tc::prefetch_tmap(&tmap_v);
-    tc::prefetch_tmap(&tmap_q);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -619,8 +622,8 @@ cudaError_t launch_t(const AttnParams& a, const CUtensorMap* tk, const CUtensorM
   cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<T, D, MT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  attn_tc_kernel<T, D, MT><<<a.sched.G, C::kThreads, C::kSmemBytes, stream>>>(*tk, *tv, *tq, a);
-  return cudaGetLastError();
+  return launch_pdl(attn_tc_kernel<T, D, MT>, dim3(a.sched.G), dim3(C::kThreads), (size_t)C::kSmemBytes, stream,
+                    *tk, *tv, *tq, a);
 }
 
 template <typename T>

@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads) cand_kernel(CandParams a) {
   const int d = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nT = a.T;
+  pdl_wait();
 
   // ---- the tree: validity, depths (pointer jumping), choice ranks ----
   if (tid == 0) {
@@ -291,11 +292,10 @@ __global__ void __launch_bounds__(kThreads) cand_kernel(CandParams a) {
 cudaError_t launch_cand(const CandParams& a, int dtype, cudaStream_t stream) {
   dim3 grid(a.heads + 1, a.B);
   switch (dtype) {
-    case 0: cand_kernel<float><<<grid, kThreads, 0, stream>>>(a); break;
-    case 1: cand_kernel<__half><<<grid, kThreads, 0, stream>>>(a); break;
-    default: cand_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(a); break;
+    case 0: return launch_pdl(cand_kernel<float>, grid, dim3(kThreads), 0, stream, a);
+    case 1: return launch_pdl(cand_kernel<__half>, grid, dim3(kThreads), 0, stream, a);
+    default: return launch_pdl(cand_kernel<__nv_bfloat16>, grid, dim3(kThreads), 0, stream, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mt

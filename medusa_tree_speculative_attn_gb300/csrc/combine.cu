@@ -12,8 +12,6 @@ namespace mt {
 
 namespace {
 
-constexpr int kMaxListed = 1024;  // pieces listed per pass
-
 // Fold one piece (max ml.x, sum ml.y, unnormalised columns v) into the running
 // result; a piece that saw no key of the row (ml.x = -inf) is skipped.
 template <int PER>
@@ -37,22 +35,32 @@ constexpr int kBlocksPerSm = 2;
 constexpr int kRound = 4;          // pieces whose loads are in flight together
 constexpr int kPfxCached = 2048;  // tile prefixes copied to shared memory up to this batch
 
-// Persistent blocks over the items (segment, 32-row block), the tile prefix
-// copied to shared memory once, so that an item whose segment was written
-// directly is skipped without a memory access.  For an item, the block lists
-// the segment's pieces; thread (warp w, lane l) merges row l for the 4-column
-// groups w, w + 8, ... (partial reads coalesced along rows), kRound pieces per
-// round with all their loads in flight; the block stages the merged rows in
-// shared memory and writes them out in 16-byte chunks along each row.
+// What a block needs to merge one item (segment, 32-row block).
+struct ItemInfo {
+  int seg, row0, nt;
+  int slot0, count;  // partial slots slot0 .. slot0 + count - 1; count 0: nothing to merge
+  int all;           // every one of those slots holds a piece
+};
+
+// Persistent blocks over the items, the tile prefix copied to shared memory
+// once.  One warp works out the next 32 items of the block at a time, a lane
+// per item (which CTAs hold pieces of the segment: 64-bit schedule arithmetic
+// in parallel instead of on every item's critical path), so that an item
+// whose segment was written directly costs nothing.  For an item, thread
+// (warp w, lane l) merges row l for the 4-column groups w, w + 8, ... (partial
+// reads coalesced along rows), kRound pieces per round with all their loads
+// in flight; the block stages the merged rows in shared memory and writes them
+// out in 16-byte chunks along each row.
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(AttnParams a) {
   constexpr int C4 = D / 4;                    // 4-column groups per row
   constexpr int PER = C4 / kWarps;             // groups per thread
   constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte output chunks per row
   __shared__ int s_pfx[kPfxCached + 1];
-  __shared__ int s_slot[kMaxListed];
+  __shared__ ItemInfo s_info[32];
   __shared__ __align__(16) T s_out[32][D + 16 / (int)sizeof(T)];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
   Sched s = a.sched;
   if (s.B <= kPfxCached) {
     for (int i = tid; i <= s.B; i += blockDim.x) s_pfx[i] = s.tile_pfx[i];
@@ -65,91 +73,98 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(Attn
   const int nrb = (PR + 31) / 32;
   const long long items = (long long)s.B * HR * nrb;
   const long long W = s.splits == 0 ? sched_total_cost(s) : 0;  // balanced mode works in cost units
-  for (long long item = blockIdx.x; item < items; item += gridDim.x) {
-    const int seg = (int)(item / nrb), row0 = (int)(item % nrb) * 32;
-    const int b = seg / HR, seg_in_b = seg % HR;
-    const int kvh = seg_in_b / s.nrg, rg = seg_in_b % s.nrg;
-    const int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
-    if (nt == 0) continue;  // invalid sequence (block-uniform)
-    // the slots holding this segment's pieces
-    int slot0, count;
+  // does partial slot slot0 + k of segment seg (nt tiles) hold a piece?
+  auto piece_exists = [&](const ItemInfo& in, int k) -> bool {
+    if (in.all || k == 0 || k == in.count - 1) return true;
     if (s.splits == 0) {
-      const long long t0 = (long long)s.tile_pfx[b] * HR + (long long)seg_in_b * nt;
-      const int c0 = sched_cta_of(sched_tile_cost(s, t0, seg), W, s.G);
-      const int c1 = sched_cta_of(sched_tile_cost(s, t0 + nt - 1, seg), W, s.G);
-      if (c0 == c1) continue;  // written directly by its only CTA
-      slot0 = seg + c0;
-      count = c1 - c0 + 1;
-    } else {
-      if (s.splits == 1) continue;
-      slot0 = seg * s.splits;
-      count = s.splits;
+      // the segment's tiles are one contiguous stretch of the cost axis: its
+      // first and last owners hold tiles of it, and a CTA in between covers its
+      // whole cost range inside it, so it holds tiles exactly when that range
+      // is not empty
+      const int c = in.slot0 - in.seg + k;
+      return W * (c + 1) / s.G > W * c / s.G;
     }
-    float M = -INFINITY, lsum = 0.f;
-    float4 acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int r = row0 + lane;
-    const bool row_ok = r < PR && rg * RG + r < a.rows;
-    for (int k0 = 0; k0 < count; k0 += kMaxListed) {
-      // list the pieces [k0, k0 + kMaxListed) that exist
-      __syncthreads();  // the previous list is no longer read
-      for (int k = k0 + tid; k < count && k < k0 + kMaxListed; k += blockDim.x) {
-        bool exists;
-        if (s.splits == 0) {
-          // the segment's tiles are one contiguous stretch of the cost axis:
-          // its first and last owners hold tiles of it, and a CTA in between
-          // covers its whole cost range inside it, so it holds tiles exactly
-          // when that range is not empty
-          const int c = slot0 - seg + k;
-          exists = k == 0 || k == count - 1 || W * (c + 1) / s.G > W * c / s.G;
-        } else {
-          exists = (long long)nt * k / s.splits < (long long)nt * (k + 1) / s.splits;
+    return (long long)in.nt * k / s.splits < (long long)in.nt * (k + 1) / s.splits;
+  };
+  for (long long base = blockIdx.x; base < items; base += 32LL * gridDim.x) {
+    __syncthreads();  // the previous batch's descriptions are no longer read
+    if (warp == 0) {
+      ItemInfo in{0, 0, 0, 0, 0, 1};
+      const long long item = base + (long long)lane * gridDim.x;
+      if (item < items) {
+        in.seg = (int)(item / nrb);
+        in.row0 = (int)(item % nrb) * 32;
+        const int b = in.seg / HR, seg_in_b = in.seg % HR;
+        in.nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
+        if (in.nt > 0 && s.splits == 0) {  // nt = 0: invalid sequence, nothing to merge
+          const long long t0 = (long long)s.tile_pfx[b] * HR + (long long)seg_in_b * in.nt;
+          const int c0 = sched_cta_of(sched_tile_cost(s, t0, in.seg), W, s.G);
+          const int c1 = sched_cta_of(sched_tile_cost(s, t0 + in.nt - 1, in.seg), W, s.G);
+          if (c0 != c1) {  // else written directly by its only CTA
+            in.slot0 = in.seg + c0;
+            in.count = c1 - c0 + 1;
+            in.all = W >= s.G;  // every CTA's cost range is non-empty
+          }
+        } else if (in.nt > 0 && s.splits > 1) {
+          in.slot0 = in.seg * s.splits;
+          in.count = s.splits;
+          in.all = in.nt >= s.splits;  // every key chunk is non-empty
         }
-        s_slot[k - k0] = exists ? slot0 + k : -1;
       }
-      __syncthreads();
-      const int n = min(kMaxListed, count - k0);
+      s_info[lane] = in;
+    }
+    __syncthreads();
+    for (int i = 0; i < 32; ++i) {
+      const ItemInfo in = s_info[i];
+      if (in.count == 0) continue;  // block-uniform
+      const int seg_in_b = in.seg % HR;
+      const int b = in.seg / HR, kvh = seg_in_b / s.nrg, rg = seg_in_b % s.nrg;
+      float M = -INFINITY, lsum = 0.f;
+      float4 acc[PER];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int r = in.row0 + lane;
+      const bool row_ok = r < PR && rg * RG + r < a.rows;
       if (row_ok) {
-        for (int k = 0; k < n; k += kRound) {
+        for (int k = 0; k < in.count; k += kRound) {
           float2 ml[kRound];
           float4 v[kRound][PER];
 #pragma unroll
           for (int j = 0; j < kRound; ++j) {
-            const int slot = k + j < n ? s_slot[k + j] : -1;
             ml[j] = make_float2(-INFINITY, 0.f);
-            if (slot >= 0) {
-              ml[j] = a.part_ml[(size_t)slot * PR + r];
+            if (k + j < in.count && piece_exists(in, k + j)) {
+              const size_t slot = (size_t)in.slot0 + k + j;
+              ml[j] = a.part_ml[slot * PR + r];
 #pragma unroll
-              for (int e = 0; e < PER; ++e) v[j][e] = a.part_o[((size_t)slot * C4 + warp + kWarps * e) * PR + r];
+              for (int e = 0; e < PER; ++e) v[j][e] = a.part_o[(slot * C4 + warp + kWarps * e) * PR + r];
             }
           }
 #pragma unroll
           for (int j = 0; j < kRound; ++j) merge<PER>(M, lsum, acc, ml[j], v[j]);
         }
       }
-    }
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      const int c = 4 * (warp + kWarps * e);
-      s_out[lane][c] = Act<T>::from_f(acc[e].x * inv);
-      s_out[lane][c + 1] = Act<T>::from_f(acc[e].y * inv);
-      s_out[lane][c + 2] = Act<T>::from_f(acc[e].z * inv);
-      s_out[lane][c + 3] = Act<T>::from_f(acc[e].w * inv);
+      for (int e = 0; e < PER; ++e) {
+        const int c = 4 * (warp + kWarps * e);
+        s_out[lane][c] = Act<T>::from_f(acc[e].x * inv);
+        s_out[lane][c + 1] = Act<T>::from_f(acc[e].y * inv);
+        s_out[lane][c + 2] = Act<T>::from_f(acc[e].z * inv);
+        s_out[lane][c + 3] = Act<T>::from_f(acc[e].w * inv);
+      }
+      __syncthreads();
+      // 32 rows x CH chunks, consecutive threads along a row
+      for (int idx = tid; idx < 32 * CH; idx += blockDim.x) {
+        const int lr = idx / CH, ch = idx % CH;
+        const int rr = in.row0 + lr;
+        const int row = rg * RG + rr;
+        if (rr >= PR || row >= a.rows) continue;
+        const int node = row / a.g, h = kvh * a.g + row % a.g;
+        T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
+        reinterpret_cast<uint4*>(dst)[ch] = *reinterpret_cast<const uint4*>(&s_out[lr][ch * (16 / sizeof(T))]);
+      }
+      __syncthreads();  // s_out is rewritten by the next item
     }
-    __syncthreads();
-    // 32 rows x CH chunks, consecutive threads along a row
-    for (int idx = tid; idx < 32 * CH; idx += blockDim.x) {
-      const int lr = idx / CH, ch = idx % CH;
-      const int rr = row0 + lr;
-      const int row = rg * RG + rr;
-      if (rr >= PR || row >= a.rows) continue;
-      const int node = row / a.g, h = kvh * a.g + row % a.g;
-      T* dst = static_cast<T*>(a.out) + (((size_t)b * a.T + node) * a.Hq + h) * D;
-      reinterpret_cast<uint4*>(dst)[ch] = *reinterpret_cast<const uint4*>(&s_out[lr][ch * (16 / sizeof(T))]);
-    }
-    __syncthreads();  // s_out is rewritten by the next item
   }
 }
 
@@ -159,8 +174,7 @@ cudaError_t launch_t(const AttnParams& a, cudaStream_t stream) {
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long items = (long long)a.B * a.Hkv * a.sched.nrg * ((a.part_rows + 31) / 32);
   const long long grid = items < (long long)kBlocksPerSm * sms ? items : (long long)kBlocksPerSm * sms;
-  combine_kernel<T, D><<<(unsigned)(grid > 0 ? grid : 1), kWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel<T, D>, dim3((unsigned)(grid > 0 ? grid : 1)), dim3(kWarps * 32), 0, stream, a);
 }
 
 }  // namespace

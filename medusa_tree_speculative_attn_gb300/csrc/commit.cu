@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitParams a, int st
   __shared__ int s_path[kMaxTree];
   __shared__ int s_L, s_len;
   const int b = blockIdx.x, tid = threadIdx.x;
+  pdl_wait();
   if (tid == 0) {
     s_L = a.accept_len[b];
     s_len = a.seq_lens[b];
@@ -38,8 +39,7 @@ __global__ void __launch_bounds__(kThreads) commit_kernel(CommitParams a, int st
 
 cudaError_t launch_commit(const CommitParams& a, cudaStream_t stream) {
   const int sv = commit_stage_vecs(a, kStageCap);
-  commit_kernel<<<a.B, kThreads, (size_t)sv * 16, stream>>>(a, sv);
-  return cudaGetLastError();
+  return launch_pdl(commit_kernel, dim3(a.B), dim3(kThreads), (size_t)sv * 16, stream, a, sv);
 }
 
 }  // namespace mt

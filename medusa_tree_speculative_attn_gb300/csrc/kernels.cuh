@@ -1,9 +1,39 @@
 // Kernel parameter blocks and launchers (internal to the library).
 #pragma once
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace mt {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation, so that its launch overlaps the
+// completion of the kernel before it on the stream.  A kernel calls
+// pdl_wait() before it reads or writes memory that an earlier kernel may
+// touch: it returns once the preceding kernel has completed and its writes
+// are visible (at once in a normal launch).  No kernel releases its successor
+// early (griddepcontrol.launch_dependents): the release happens as its CTAs
+// exit, so every earlier kernel has completed when a successor starts.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct PrepParams {
   int B, T, Hq, Hkv, D, P, max_blocks, num_pages, max_pos;

@@ -136,6 +136,7 @@ __device__ void ancestor_masks(const PrepParams& a, int b, unsigned long long* s
 template <typename T>
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
   const int tid = threadIdx.x;
+  pdl_wait();
   if (blockIdx.x == 0) {
     // ---- schedule block (block 0: dispatched first): tree and length
     // checks, tiles per segment, their prefix, and the CTAs' piece lists.
@@ -332,11 +333,10 @@ cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream) {
   if (smem > 48 * 1024) return cudaErrorInvalidValue;
   dim3 grid((unsigned)blocks);
   switch (dtype) {
-    case 0: prep_kernel<float><<<grid, kPrepThreads, smem, stream>>>(a); break;
-    case 1: prep_kernel<__half><<<grid, kPrepThreads, smem, stream>>>(a); break;
-    default: prep_kernel<__nv_bfloat16><<<grid, kPrepThreads, smem, stream>>>(a); break;
+    case 0: return launch_pdl(prep_kernel<float>, grid, dim3(kPrepThreads), smem, stream, a);
+    case 1: return launch_pdl(prep_kernel<__half>, grid, dim3(kPrepThreads), smem, stream, a);
+    default: return launch_pdl(prep_kernel<__nv_bfloat16>, grid, dim3(kPrepThreads), smem, stream, a);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace mt
