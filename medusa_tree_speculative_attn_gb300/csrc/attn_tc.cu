@@ -345,6 +345,9 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         wait_all(&full[stage], (it / S) & 1);
         if (!ok) break;
         const uint32_t k_u = sKV_u + stage * C::kStageBytes;
+        // one descriptor per stage; a K slice is a constant offset (16-byte
+        // units in the address field, which cannot carry: addresses < 256 KB)
+        const uint64_t kd0 = tc::smem_desc(k_u, 16, 1024);
         for (int m = 0; m < MT; ++m) {
           // S_m held the scores of tile it - 1 until the softmax read them
           if (it >= 1) {
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t h = kk / 4, k4 = kk % 4;
-              const uint64_t bd = tc::smem_desc(k_u + h * C::kHalfTile + k4 * 32, 16, 1024);
+              const uint64_t bd = kd0 + (uint64_t)((h * C::kHalfTile + k4 * 32) >> 4);
               if (kk == 0) tc::mma_f16_ts<false>(tmem + C::s_col(m), tmem + C::q_col(m) + kk * 8, bd, kIdescQK);
               else tc::mma_f16_ts<true>(tmem + C::s_col(m), tmem + C::q_col(m) + kk * 8, bd, kIdescQK);
             }
@@ -416,16 +419,14 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
           if (lane == 0) {
             const uint32_t d_t = tmem + C::o_col(m);
             const uint32_t p_u = sP_u + m * C::kPTile;
+            const uint64_t pd0 = tc::smem_desc(p_u, 16, 1024), vd0 = tc::smem_desc(v_u, C::kHalfTile, 1024);
             if (first)
-              tc::mma_f16_ss<false>(d_t, tc::smem_desc(p_u, 16, 1024), tc::smem_desc(v_u, C::kHalfTile, 1024),
-                                    kIdescPV);
+              tc::mma_f16_ss<false>(d_t, pd0, vd0, kIdescPV);
             else
-              tc::mma_f16_ss<true>(d_t, tc::smem_desc(p_u, 16, 1024), tc::smem_desc(v_u, C::kHalfTile, 1024),
-                                   kIdescPV);
+              tc::mma_f16_ss<true>(d_t, pd0, vd0, kIdescPV);
 #pragma unroll
-            for (int kk = 1; kk < kTileKeys / 16; ++kk)
-              tc::mma_f16_ss<true>(d_t, tc::smem_desc(p_u + kk * 32, 16, 1024),
-                                   tc::smem_desc(v_u + kk * 2048, C::kHalfTile, 1024), kIdescPV);
+            for (int kk = 1; kk < kTileKeys / 16; ++kk)  // next 16 keys: P +32 B, V +2048 B
+              tc::mma_f16_ss<true>(d_t, pd0 + (uint64_t)(kk * 2), vd0 + (uint64_t)(kk * 128), kIdescPV);
             tc::mma_commit(&pv_done[m]);
           }
           __syncwarp();

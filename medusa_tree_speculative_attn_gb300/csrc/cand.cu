@@ -10,9 +10,10 @@
 //   among equal values".
 // One CTA per (depth, sequence): CTA (0, b) takes the root's argmax, CTA (d, b)
 // the top kMaxChoices of head d - 1, and each writes the tokens of its nodes.
-// A row is read twice with 16-byte loads (the second pass from L2): the first
-// pass takes each thread's maximum, and tau = the k-th largest of those
-// maxima bounds the k best entries from below (k thread maxima are >= tau);
+// A row is read twice with 16-byte loads, eight in flight per thread (the
+// second pass from L2): the first pass takes each thread's maximum, and tau =
+// the k-th largest of those maxima bounds the k best entries from below (k
+// thread maxima are >= tau);
 // the second pass collects the entries >= tau in shared memory, and each
 // candidate's rank among them (an O(n^2) count in the stated order) places the
 // k best.  When ties put more than kCand entries at or above tau, the block
@@ -26,6 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCand = 512;  // candidates collected above the threshold
+constexpr int kBatch = 8;   // 16-byte loads in flight per thread
 
 // (value, index) order: larger value first, lower index among equal values.
 __device__ __forceinline__ bool before(float v, int i, float w, int j) {
@@ -153,10 +155,17 @@ __global__ void __launch_bounds__(kThreads) cand_kernel(CandParams a) {
   // ---- fast path: threshold, then the entries at or above it ----
   {
     float tm = -INFINITY;
-    for (int v = tid; v < nvec; v += kThreads) {
-      const uint4 raw = reinterpret_cast<const uint4*>(row)[v];
+    for (int v0 = tid; v0 < nvec; v0 += kThreads * kBatch) {
+      uint4 raw[kBatch];
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) tm = fmaxf(tm, Vec<T>::at(raw, e));
+      for (int j = 0; j < kBatch; ++j)
+        if (v0 + j * kThreads < nvec) raw[j] = reinterpret_cast<const uint4*>(row)[v0 + j * kThreads];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j)
+        if (v0 + j * kThreads < nvec) {
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) tm = fmaxf(tm, Vec<T>::at(raw[j], e));
+        }
     }
     for (int i = nvec * EPV + tid; i < a.V; i += kThreads) tm = fmaxf(tm, Act<T>::to_f(row[i]));
     s_tm[tid] = tm;
@@ -168,16 +177,24 @@ __global__ void __launch_bounds__(kThreads) cand_kernel(CandParams a) {
     if (rk == kneed - 1) s_tau = tm;
     __syncthreads();
     const float tau = s_tau;
-    for (int v = tid; v < nvec; v += kThreads) {
-      const uint4 raw = reinterpret_cast<const uint4*>(row)[v];
+    for (int v0 = tid; v0 < nvec; v0 += kThreads * kBatch) {
+      uint4 raw[kBatch];
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const float x = Vec<T>::at(raw, e);
-        if (x >= tau) {
-          const int slot = atomicAdd(&s_cnt, 1);
-          if (slot < kCand) {
-            s_cv[slot] = x;
-            s_ci[slot] = v * EPV + e;
+      for (int j = 0; j < kBatch; ++j)
+        if (v0 + j * kThreads < nvec) raw[j] = reinterpret_cast<const uint4*>(row)[v0 + j * kThreads];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = v0 + j * kThreads;
+        if (v >= nvec) continue;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          const float x = Vec<T>::at(raw[j], e);
+          if (x >= tau) {
+            const int slot = atomicAdd(&s_cnt, 1);
+            if (slot < kCand) {
+              s_cv[slot] = x;
+              s_ci[slot] = v * EPV + e;
+            }
           }
         }
       }
