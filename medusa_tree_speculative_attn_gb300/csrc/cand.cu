@@ -12,8 +12,8 @@
 // the top kMaxChoices of head d - 1, and each writes the tokens of its nodes.
 // A row is read twice with 16-byte loads, eight in flight per thread (the
 // second pass from L2): the first pass takes each thread's maximum, and tau =
-// the k-th largest of those maxima bounds the k best entries from below (k
-// thread maxima are >= tau);
+// the largest over warps of each warp's k-th largest thread maximum bounds the
+// k best entries from below (k thread maxima of that warp are >= tau);
 // the second pass collects the entries >= tau in shared memory, and each
 // candidate's rank among them (an O(n^2) count in the stated order) places the
 // k best.  When ties put more than kCand entries at or above tau, the block
@@ -82,11 +82,10 @@ __global__ void __launch_bounds__(kThreads) cand_kernel(CandParams a) {
   __shared__ float s_wv[kWarps][K];
   __shared__ int s_wi[kWarps][K];
   __shared__ int s_top[K];
-  __shared__ float s_tm[kThreads];
+  __shared__ float s_wt[kWarps];
   __shared__ float s_cv[kCand];
   __shared__ int s_ci[kCand];
   __shared__ int s_cnt;
-  __shared__ float s_tau;
   const int d = blockIdx.x, b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nT = a.T;
@@ -168,15 +167,19 @@ __global__ void __launch_bounds__(kThreads) cand_kernel(CandParams a) {
         }
     }
     for (int i = nvec * EPV + tid; i < a.V; i += kThreads) tm = fmaxf(tm, Act<T>::to_f(row[i]));
-    s_tm[tid] = tm;
+    // tau: for each warp the kneed-th largest of its 32 thread maxima (rank by
+    // value, ties by lane), then the largest of those over the warps: kneed
+    // entries of one warp's slice are >= tau, and tau is at most the kneed-th
+    // largest of all the maxima
+    int rk = 0;
+#pragma unroll
+    for (int l = 0; l < 32; ++l) rk += before(__shfl_sync(0xffffffffu, tm, l), l, tm, lane);
+    if (rk == kneed - 1) s_wt[warp] = tm;
     if (tid == 0) s_cnt = 0;
     __syncthreads();
-    // tau: the kneed-th largest thread maximum (ties among maxima by thread)
-    int rk = 0;
-    for (int u = 0; u < kThreads; ++u) rk += before(s_tm[u], u, tm, tid);
-    if (rk == kneed - 1) s_tau = tm;
-    __syncthreads();
-    const float tau = s_tau;
+    float tau = s_wt[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) tau = fmaxf(tau, s_wt[w]);
     for (int v0 = tid; v0 < nvec; v0 += kThreads * kBatch) {
       uint4 raw[kBatch];
 #pragma unroll
