@@ -50,6 +50,8 @@ def _load():
             i32, i64, dbl = ctypes.c_int, ctypes.c_long, ctypes.c_double
             lib.or_round_to_act.argtypes = [i32, i64, P, P]
             lib.or_act_to_double.argtypes = [i32, i64, P, P]
+            lib.or_e4m3_encode_array.argtypes = [i64, P, P]
+            lib.or_e4m3_decode_array.argtypes = [i64, P, P]
             lib.or_num_threads.restype = i32
             lib.or_rope_table.argtypes = [dbl, i32, i32, P, P]
             lib.or_rope_rotate.argtypes = [i32, i64, i32, P, P, i32, P, P, P]
@@ -99,6 +101,23 @@ def round_to_act(x: np.ndarray, dtype: str) -> np.ndarray:
     x = np.ascontiguousarray(x, dtype=np.float32)
     out = np.empty(x.shape, dtype={"f32": np.float32, "f16": np.float16, "bf16": np.uint16}[dtype])
     _load().or_round_to_act(DTYPES[dtype], x.size, _ptr(x), _ptr(out))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """FP8 E4M3 codes (uint8) of float64 values: nearest, ties to the even code,
+    finite overflow and infinities saturated to +-448, NaN kept."""
+    x = np.ascontiguousarray(x, np.float64)
+    out = np.empty(x.shape, np.uint8)
+    _load().or_e4m3_encode_array(x.size, _ptr(x), _ptr(out))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 values of FP8 E4M3 codes."""
+    codes = np.ascontiguousarray(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _load().or_e4m3_decode_array(codes.size, _ptr(codes), _ptr(out))
     return out
 
 

@@ -27,11 +27,13 @@
  * Readings the pages leave open (the node-0 root at position prefix_len,
  * self-visibility, NeoX half-split RoPE pairing, 1/sqrt(D) scale, lowest index
  * on argmax ties, deepest-then-lowest-index path end, ascending-depth commit,
- * release of scratch pages past the new length) are stated at each function.
+ * release of scratch pages past the new length, the FP8 E4M3 element format of
+ * an FP8 KV cache) are stated at each function.
  *
  * Parity pins: every function here is checked by tests that do not re-type its
  * formula (dense-mask brute force, closed forms, invariants, exhaustive
- * enumeration, hand-derived fixtures).  No function is "parity unpinned".
+ * enumeration, hand-derived fixtures, a library's own conversion).  No function
+ * is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
@@ -129,6 +131,54 @@ void or_round_to_act(int dt, long n, const float* x, void* y) {
 /* Exposed for the tests: decode act-dtype values to float64. */
 void or_act_to_double(int dt, long n, const void* x, double* y) {
   for (long i = 0; i < n; ++i) y[i] = load_act(dt, x, (size_t)i);
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8 E4M3 (OCP 8-bit floating point, the variant without infinities), the  */
+/* element format of an FP8 KV cache.  Reading (the pages define no FP8      */
+/* cache): bits S EEEE MMM, exponent bias 7; E = 0 is subnormal,             */
+/* (-1)^S 2^-6 M/8; otherwise (-1)^S 2^(E-7) (1 + M/8); S 1111 111 is NaN,   */
+/* so the largest finite magnitude is 2^8 * 1.75 = 448.  Encoding rounds to  */
+/* the nearest representable value, ties to the even code (mantissa LSB 0),  */
+/* and saturates finite overflow and infinities to +-448; NaN stays NaN.     */
+/* ------------------------------------------------------------------------- */
+
+static double e4m3_magnitude(int code7) {  /* code7 = E:M, 0 .. 0x7E */
+  int E = code7 >> 3, M = code7 & 7;
+  return E == 0 ? ldexp((double)M / 8.0, -6) : ldexp(1.0 + (double)M / 8.0, E - 7);
+}
+
+double or_e4m3_decode(int code) {
+  int sign = (code >> 7) & 1, mag = code & 0x7F;
+  if (mag == 0x7F) return NAN;
+  double v = e4m3_magnitude(mag);
+  return sign ? -v : v;
+}
+
+int or_e4m3_encode(double x) {
+  if (isnan(x)) return 0x7F;
+  int sign = signbit(x) ? 0x80 : 0;
+  double a = fabs(x);
+  if (a >= 448.0) return sign | 0x7E;
+  /* the nearest of the 127 finite magnitudes; on a tie the even code */
+  int best = 0;
+  double best_d = a;
+  for (int c = 1; c <= 0x7E; ++c) {
+    double d = fabs(e4m3_magnitude(c) - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  return sign | best;
+}
+
+/* Exposed for the tests: arrays of codes and values. */
+void or_e4m3_encode_array(long n, const double* x, uint8_t* codes) {
+  for (long i = 0; i < n; ++i) codes[i] = (uint8_t)or_e4m3_encode(x[i]);
+}
+void or_e4m3_decode_array(long n, const uint8_t* codes, double* x) {
+  for (long i = 0; i < n; ++i) x[i] = or_e4m3_decode(codes[i]);
 }
 
 int or_num_threads(void) {
