@@ -27,7 +27,7 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}  # e4m3: FP8 cache elements (codes)
 
 
 def build(force: bool = False) -> str:
@@ -51,6 +51,8 @@ def _load():
             lib.or_round_to_act.argtypes = [i32, i64, P, P]
             lib.or_act_to_double.argtypes = [i32, i64, P, P]
             lib.or_e4m3_encode_array.argtypes = [i64, P, P]
+            lib.or_tree_scatter_e4m3.argtypes = [i32] * 8 + [P] * 6 + [ctypes.c_float, ctypes.c_float]
+            lib.or_tree_attn_e4m3.argtypes = [i32] * 9 + [P] * 3 + [dbl, dbl] + [P] * 3 + [dbl, i64, P, P]
             lib.or_e4m3_decode_array.argtypes = [i64, P, P]
             lib.or_num_threads.restype = i32
             lib.or_rope_table.argtypes = [dbl, i32, i32, P, P]
@@ -216,6 +218,51 @@ def tree_scatter(w: dict, k_cache: np.ndarray, v_cache: np.ndarray, k_rot=None):
     return kc, vc
 
 
+def tree_scatter_e4m3(w: dict, k_codes: np.ndarray, v_codes: np.ndarray, k_scale: float,
+                      v_scale: float, k_rot=None):
+    """An FP8 cache (E4M3 codes, uint8) after the attention call: at slots len+i,
+    the codes of the act-dtype rotated key / raw value divided by its scale in
+    float32."""
+    if k_rot is None:
+        _, k_rot = rotate_inputs(w)
+    kc = np.ascontiguousarray(k_codes, np.uint8).copy()
+    vc = np.ascontiguousarray(v_codes, np.uint8).copy()
+    st = _load().or_tree_scatter_e4m3(DTYPES[w["dtype"]], w["B"], w["T"], w["Hkv"], w["head_dim"],
+                                      w["page_size"], w["max_blocks"], w["num_pages"], _ptr(k_rot),
+                                      _ptr(_act(w["v_new"], w["dtype"])), _ptr(kc), _ptr(vc),
+                                      _ptr(_i32(w["block_tables"])), _ptr(_i32(w["seq_lens"])),
+                                      float(k_scale), float(v_scale))
+    _check(st, "tree_scatter_e4m3")
+    return kc, vc
+
+
+def tree_attn_e4m3(w: dict, k_codes: np.ndarray, v_codes: np.ndarray, k_scale: float, v_scale: float,
+                   sel=None, q_rot=None) -> np.ndarray:
+    """Attention outputs (float64) over an FP8 cache that already holds the tree's
+    K/V (tree_scatter_e4m3): every visible slot, prefix and tree, read as
+    decode(code) * scale.  sel as in tree_attn."""
+    B, T, Hq, Hkv, D = w["B"], w["T"], w["Hq"], w["Hkv"], w["head_dim"]
+    if q_rot is None:
+        q_rot, _ = rotate_inputs(w)
+    full = sel is None
+    if full:
+        bb, ii, hh = np.meshgrid(np.arange(B), np.arange(T), np.arange(Hq), indexing="ij")
+        sel = np.stack([bb.ravel(), hh.ravel(), ii.ravel()], axis=1)
+    sel = _i32(sel).reshape(-1, 3)
+    out = np.empty((sel.shape[0], D), dtype=np.float64)
+    scale = w.get("sm_scale") or 1.0 / np.sqrt(D)
+    st = _load().or_tree_attn_e4m3(DTYPES[w["dtype"]], B, T, Hq, Hkv, D, w["page_size"], w["max_blocks"],
+                                   w["num_pages"], _ptr(q_rot), _ptr(np.ascontiguousarray(k_codes, np.uint8)),
+                                   _ptr(np.ascontiguousarray(v_codes, np.uint8)), float(k_scale),
+                                   float(v_scale), _ptr(_i32(w["block_tables"])), _ptr(_i32(w["seq_lens"])),
+                                   _ptr(_i32(w["tree_parents"])), float(scale), sel.shape[0], _ptr(sel),
+                                   _ptr(out))
+    _check(st, "tree_attn_e4m3")
+    if full:
+        return out.reshape(B, T, Hq, D)
+    return out
+
+
 def accept_greedy(tokens, logits: np.ndarray, logits_dtype: str, parents, max_depth: int):
     """Returns (argmax [B,T], accept_len [B], accept_path [B,max_depth+1], next_token [B])."""
     tokens = _i32(tokens)
@@ -253,15 +300,16 @@ def released_width(T: int, page_size: int) -> int:
 
 
 def kv_commit(w: dict, accept_path, accept_len, k_cache, v_cache, block_tables, seq_lens,
-              max_depth: int):
-    """Returns the committed (k_cache, v_cache, block_tables, seq_lens, released_pages)."""
+              max_depth: int, cache_dtype: str = None):
+    """Returns the committed (k_cache, v_cache, block_tables, seq_lens, released_pages).
+    cache_dtype: the cache's element type when it is not the act dtype ("e4m3")."""
     kc = np.ascontiguousarray(k_cache).copy()
     vc = np.ascontiguousarray(v_cache).copy()
     bt = _i32(block_tables).copy()
     sl = _i32(seq_lens).copy()
     width = released_width(w["T"], w["page_size"])
     rel = np.empty((w["B"], width), np.int32)
-    st = _load().or_kv_commit(DTYPES[w["dtype"]], w["B"], w["T"], w["Hkv"], w["head_dim"],
+    st = _load().or_kv_commit(DTYPES[cache_dtype or w["dtype"]], w["B"], w["T"], w["Hkv"], w["head_dim"],
                               w["page_size"], w["max_blocks"], w["num_pages"], max_depth,
                               _ptr(_i32(accept_path)), _ptr(_i32(accept_len)), _ptr(kc), _ptr(vc),
                               _ptr(bt), _ptr(sl), _ptr(rel), width)

@@ -43,7 +43,7 @@
 #include <omp.h>
 #endif
 
-enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2 };
+enum { OR_F32 = 0, OR_F16 = 1, OR_BF16 = 2, OR_E4M3 = 3 /* FP8 cache element */ };
 enum { OR_OK = 0, OR_ERR_ARG = -1, OR_ERR_TREE = -3, OR_ERR_PAGES = -4 };
 
 /* ------------------------------------------------------------------------- */
@@ -109,7 +109,7 @@ static uint16_t float_to_bf16_bits(float f) {
   return encode_binary16_like(r, 7, -126, 127, 8);
 }
 
-static size_t elem_size(int dt) { return dt == OR_F32 ? 4 : 2; }
+static size_t elem_size(int dt) { return dt == OR_F32 ? 4 : dt == OR_E4M3 ? 1 : 2; }
 
 static double load_act(int dt, const void* base, size_t i) {
   if (dt == OR_F32) return (double)((const float*)base)[i];
@@ -399,6 +399,105 @@ int or_tree_scatter(int dt, int B, int T, int Hkv, int D, int P, int max_blocks,
  *   accept_path[b] = node ids root..end, then -1 up to max_depth+1 entries;
  *   next_token[b]  = am[end] (the token the target model adds after the path).
  * Logits are fp32/fp16/bf16 [B][T][V]; no NaNs (precondition). */
+/* ------------------------------------------------------------------------- */
+/* FP8 KV cache (reading; the pages define no FP8 cache): the cache holds    */
+/* E4M3 codes of value / scale, one scale for all of K and one for all of V; */
+/* a cached element stands for decode(code) * scale.                         */
+/* ------------------------------------------------------------------------- */
+
+/* Tree K/V into an FP8 cache at logical slots L_b + i: the act-dtype rotated
+ * key (raw value) divided by its scale in float32, then encoded. */
+int or_tree_scatter_e4m3(int dt, int B, int T, int Hkv, int D, int P, int max_blocks, int num_pages,
+                         const void* k_rot, const void* v_new, uint8_t* k_cache, uint8_t* v_cache,
+                         const int32_t* block_tables, const int32_t* seq_lens, float k_scale,
+                         float v_scale) {
+  if (!(k_scale > 0.0f) || !(v_scale > 0.0f)) return OR_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    for (int i = 0; i < T; ++i) {
+      for (int kvh = 0; kvh < Hkv; ++kvh) {
+        long off = slot_offset(block_tables, max_blocks, num_pages, Hkv, P, D, b, kvh,
+                               (long)seq_lens[b] + i);
+        if (off < 0) return OR_ERR_PAGES;
+        size_t src = (((size_t)b * T + i) * Hkv + kvh) * D;
+        for (int d = 0; d < D; ++d) {
+          float xk = (float)load_act(dt, k_rot, src + d);
+          float xv = (float)load_act(dt, v_new, src + d);
+          k_cache[(size_t)off + d] = (uint8_t)or_e4m3_encode((double)(xk / k_scale));
+          v_cache[(size_t)off + d] = (uint8_t)or_e4m3_encode((double)(xv / v_scale));
+        }
+      }
+    }
+  }
+  return OR_OK;
+}
+
+/* Tree attention over an FP8 cache: node i of sequence b sees the prefix
+ * slots [0, L_b) and the tree slots L_b + t of its own root path, every one
+ * read from the cache (so the tree's keys and values too are the encoded
+ * ones); softmax(q . k * sm_scale) v in float64 with k, v = decode * scale.
+ * q_rot is the act-dtype rotated query.  Same selection and output layout as
+ * or_tree_attn. */
+int or_tree_attn_e4m3(int dt, int B, int T, int Hq, int Hkv, int D, int P, int max_blocks,
+                      int num_pages, const void* q_rot, const uint8_t* k_cache,
+                      const uint8_t* v_cache, double k_scale, double v_scale,
+                      const int32_t* block_tables, const int32_t* seq_lens, const int32_t* parents,
+                      double sm_scale, long n_sel, const int32_t* sel, double* out) {
+  if (Hkv <= 0 || Hq % Hkv != 0 || D <= 0 || P <= 0) return OR_ERR_ARG;
+  int g = Hq / Hkv;
+  for (int b = 0; b < B; ++b) {
+    int st = check_tree(T, parents + (size_t)b * T, NULL);
+    if (st) return st;
+  }
+  int status = OR_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long n = 0; n < n_sel; ++n) {
+    int b = sel[3 * n], h = sel[3 * n + 1], i = sel[3 * n + 2];
+    int kvh = h / g;
+    long L = seq_lens[b];
+    const int32_t* par = parents + (size_t)b * T;
+    /* the visible slots: the prefix, then the root-to-node path of i */
+    long nvis = L;
+    long* slot = (long*)malloc(sizeof(long) * (size_t)(L + 65));
+    for (long j = 0; j < L; ++j) slot[j] = j;
+    for (int a = i; a >= 0 && nvis < L + 65; a = par[a]) slot[nvis++] = L + a;
+    long* koff = (long*)malloc(sizeof(long) * (size_t)nvis);
+    double* s = (double*)malloc(sizeof(double) * (size_t)nvis);
+    double* q = (double*)malloc(sizeof(double) * (size_t)D);
+    for (int d = 0; d < D; ++d) q[d] = load_act(dt, q_rot, (((size_t)b * T + i) * Hq + h) * D + d);
+    int bad = 0;
+    for (long j = 0; j < nvis; ++j) {
+      koff[j] = slot_offset(block_tables, max_blocks, num_pages, Hkv, P, D, b, kvh, slot[j]);
+      if (koff[j] < 0) bad = 1;
+    }
+    if (bad) {
+#pragma omp critical
+      status = OR_ERR_PAGES;
+    } else {
+      double smax = -INFINITY;
+      for (long j = 0; j < nvis; ++j) {
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d) dot += q[d] * (or_e4m3_decode(k_cache[(size_t)koff[j] + d]) * k_scale);
+        s[j] = dot * sm_scale;
+        if (s[j] > smax) smax = s[j];
+      }
+      double denom = 0.0;
+      double* o = out + (size_t)n * D;
+      for (int d = 0; d < D; ++d) o[d] = 0.0;
+      for (long j = 0; j < nvis; ++j) {
+        double p = exp(s[j] - smax);
+        denom += p;
+        for (int d = 0; d < D; ++d) o[d] += p * (or_e4m3_decode(v_cache[(size_t)koff[j] + d]) * v_scale);
+      }
+      for (int d = 0; d < D; ++d) o[d] /= denom;
+    }
+    free(slot);
+    free(koff);
+    free(s);
+    free(q);
+  }
+  return status;
+}
+
 int or_accept_greedy(int dt, int B, int T, int V, int max_depth, const int32_t* tokens,
                      const void* logits, const int32_t* parents, int32_t* argmax_out,
                      int32_t* accept_len, int32_t* accept_path, int32_t* next_token) {
