@@ -80,7 +80,8 @@ typedef enum {
   MT_ERR_TIMEOUT = -6       /* (device) a bounded pipeline wait gave up */
 } mt_status;
 
-typedef enum { MT_F32 = 0, MT_F16 = 1, MT_BF16 = 2 } mt_dtype;
+/* MT_E4M3 is a cache element type only (see mt_attn_desc.cache_dtype). */
+typedef enum { MT_F32 = 0, MT_F16 = 1, MT_BF16 = 2, MT_E4M3 = 3 } mt_dtype;
 
 /* Kernel choice for mt_tree_attn_paged.  AUTO: tensor cores (tcgen05, TMEM,
  * TMA) for fp16/bf16, the SIMT kernel for fp32.  SIMT: the CUDA-core kernel for
@@ -100,9 +101,24 @@ typedef struct {
                               persistent CTA takes an equal share of all key
                               tiles); n > 0: every (sequence, KV head) is split
                               into n key chunks merged by a log-sum-exp pass */
-  mt_dtype dtype;          /* q, k_new, v_new, caches and out */
+  mt_dtype dtype;          /* q, k_new, v_new, out, and the caches unless cache_dtype says
+                              otherwise */
   float sm_scale;          /* softmax scale; 0 means 1/sqrt(D) */
   int kernel;              /* an mt_kernel value */
+  /* FP8 KV cache (a reading: the pages this library follows define none).
+   * cache_dtype 0: the caches hold dtype.  MT_E4M3: they hold OCP FP8 E4M3
+   * codes (no infinities; largest finite 448) of value / scale, one scale for
+   * K and one for V, and every cached element stands for decode(code) *
+   * scale, the tree's own K/V included: mt_tree_attn_paged writes the code of
+   * (act-rounded rotated key or raw value) / scale, divided in fp32 and
+   * rounded to nearest even with saturation to +-448, and reads every visible
+   * slot back through the scale.  Runs on the SIMT kernel (MT_KERNEL_TC is
+   * unsupported with it); mt_kv_commit and mt_tree_accept_commit move the
+   * 1-byte elements.  k_scale, v_scale: positive and finite for MT_E4M3,
+   * ignored otherwise. */
+  int cache_dtype;
+  float k_scale;
+  float v_scale;
 } mt_attn_desc;
 
 /* ---- RoPE table ----------------------------------------------------------

@@ -27,6 +27,7 @@ LIB_PATH = os.path.join(_HERE, "lib", "libmedusa_tree.so")
 MT_OK = 0
 KERNELS = {"auto": 0, "simt": 1, "tc": 2}
 _DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+MT_E4M3 = 3  # cache element type: OCP FP8 E4M3 codes (torch.float8_e4m3fn)
 
 
 class MedusaTreeError(RuntimeError):
@@ -41,7 +42,9 @@ class AttnDesc(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("page_size", ctypes.c_int),
                 ("max_blocks_per_seq", ctypes.c_int), ("num_pages", ctypes.c_int),
                 ("num_splits", ctypes.c_int), ("dtype", ctypes.c_int),
-                ("sm_scale", ctypes.c_float), ("kernel", ctypes.c_int)]
+                ("sm_scale", ctypes.c_float), ("kernel", ctypes.c_int),
+                ("cache_dtype", ctypes.c_int), ("k_scale", ctypes.c_float),
+                ("v_scale", ctypes.c_float)]
 
 
 _lib = None
@@ -128,14 +131,31 @@ class Rope:
             self.handle = ctypes.c_void_p()
 
 
+def _fp8(cache: torch.Tensor) -> bool:
+    return cache.dtype == torch.float8_e4m3fn
+
+
 def make_desc(q: torch.Tensor, k_cache: torch.Tensor, block_tables: torch.Tensor,
-              num_splits: int = 0, kernel: str = "auto", sm_scale: float = 0.0) -> AttnDesc:
+              num_splits: int = 0, kernel: str = "auto", sm_scale: float = 0.0,
+              k_scale: float = 1.0, v_scale: float = 1.0) -> AttnDesc:
+    """The call's descriptor; an FP8 E4M3 cache (torch.float8_e4m3fn) holds the
+    codes of value / k_scale (keys) and value / v_scale (values)."""
     B, T, Hq, D = q.shape
     num_pages, Hkv, P, D2 = k_cache.shape
     if D2 != D:
         raise ValueError("q and k_cache head_dim differ")
     return AttnDesc(B, T, Hq, Hkv, D, P, block_tables.shape[1], num_pages, int(num_splits),
-                    _DTYPES[q.dtype], float(sm_scale), KERNELS[kernel])
+                    _DTYPES[q.dtype], float(sm_scale), KERNELS[kernel],
+                    MT_E4M3 if _fp8(k_cache) else 0, float(k_scale), float(v_scale))
+
+
+def _commit_desc(B: int, T: int, k_cache: torch.Tensor, max_blocks: int) -> AttnDesc:
+    num_pages, Hkv, P, D = k_cache.shape
+    if _fp8(k_cache):   # the act dtype does not matter to a commit: bytes move as they are
+        return AttnDesc(B, T, Hkv, Hkv, D, P, max_blocks, num_pages, 0, _DTYPES[torch.bfloat16],
+                        0.0, 0, MT_E4M3, 1.0, 1.0)
+    return AttnDesc(B, T, Hkv, Hkv, D, P, max_blocks, num_pages, 0, _DTYPES[k_cache.dtype], 0.0, 0,
+                    0, 1.0, 1.0)
 
 
 def attn_workspace_size(desc: AttnDesc) -> int:
@@ -159,18 +179,23 @@ def alloc_accept_workspace(batch: int, tree_size: int, device="cuda") -> torch.T
 
 def tree_attn_paged(q, k_cache, v_cache, block_tables, seq_lens, tree_parents, tree_depths, out, *,
                     k_new, v_new, rope: Rope, workspace: torch.Tensor, num_splits: int = 0,
-                    kernel: str = "auto", sm_scale: float = 0.0, stream=None):
-    """out[b,i,h] = attention of tree node i (head h) over the prefix + its ancestors."""
+                    kernel: str = "auto", sm_scale: float = 0.0, k_scale: float = 1.0,
+                    v_scale: float = 1.0, stream=None):
+    """out[b,i,h] = attention of tree node i (head h) over the prefix + its ancestors.
+
+    The caches hold q's dtype, or FP8 E4M3 codes (torch.float8_e4m3fn) of
+    value / k_scale and value / v_scale, read on the CUDA-core kernel."""
     for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("out", out)):
         _need(t, name, q.dtype, 4)
+    cache_dtype = torch.float8_e4m3fn if _fp8(k_cache) else q.dtype
     for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
-        _need(t, name, q.dtype, 4)
+        _need(t, name, cache_dtype, 4)
     for name, t in (("block_tables", block_tables), ("tree_parents", tree_parents),
                     ("tree_depths", tree_depths)):
         _need(t, name, torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     _need(workspace, "workspace")
-    desc = make_desc(q, k_cache, block_tables, num_splits, kernel, sm_scale)
+    desc = make_desc(q, k_cache, block_tables, num_splits, kernel, sm_scale, k_scale, v_scale)
     st = _load().mt_tree_attn_paged(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new),
                                     _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                     _ptr(seq_lens), _ptr(tree_parents), _ptr(tree_depths),
@@ -220,12 +245,11 @@ def kv_commit(accept_path, accept_len, k_cache, v_cache, block_tables, seq_lens,
     _need(released_pages, "released_pages", torch.int32, 2)
     _need(k_cache, "k_cache", None, 4)
     _need(v_cache, "v_cache", k_cache.dtype, 4)
-    num_pages, Hkv, P, D = k_cache.shape
+    P = k_cache.shape[2]
     B = block_tables.shape[0]
     if released_pages.shape != (B, released_width(tree_size, P)):
         raise ValueError("released_pages must be [B, (T + 2P - 2) // P]")
-    desc = AttnDesc(B, int(tree_size), Hkv, Hkv, D, P, block_tables.shape[1], num_pages, 0,
-                    _DTYPES[k_cache.dtype], 0.0, 0)
+    desc = _commit_desc(B, int(tree_size), k_cache, block_tables.shape[1])
     st = _load().mt_kv_commit(ctypes.byref(desc), accept_path.shape[1] - 1, _ptr(accept_path),
                               _ptr(accept_len), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                               _ptr(seq_lens), _ptr(released_pages), _ptr(status_ws), _stream(stream))
@@ -253,11 +277,10 @@ def tree_accept_commit(tree_tokens, target_logits, tree_parents, accept_len, acc
         max_depth = accept_path.shape[1] - 1
     if accept_path.shape[1] != max_depth + 1:
         raise ValueError("accept_path must have max_depth + 1 columns")
-    num_pages, Hkv, P, D = k_cache.shape
+    P = k_cache.shape[2]
     if released_pages.shape != (B, released_width(T, P)):
         raise ValueError("released_pages must be [B, (T + 2P - 2) // P]")
-    desc = AttnDesc(B, int(T), Hkv, Hkv, D, P, block_tables.shape[1], num_pages, 0,
-                    _DTYPES[k_cache.dtype], 0.0, 0)
+    desc = _commit_desc(B, int(T), k_cache, block_tables.shape[1])
     st = _load().mt_tree_accept_commit(ctypes.byref(desc), V, int(max_depth),
                                        _DTYPES[target_logits.dtype], _ptr(tree_tokens),
                                        _ptr(target_logits), _ptr(tree_parents), _ptr(argmax_out),

@@ -33,9 +33,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 
 int elem_bytes(mt_dtype dt) { return dt == MT_F32 ? 4 : 2; }
 
+bool fp8_cache(const mt_attn_desc* d) { return d->cache_dtype == MT_E4M3; }
+
+// Bytes of one cache element.
+int cache_elem_bytes(const mt_attn_desc* d) { return fp8_cache(d) ? 1 : elem_bytes(d->dtype); }
+
 // Which attention kernel a descriptor runs.
 int select_kernel(const mt_attn_desc* d) {
-  if (d->kernel == MT_KERNEL_SIMT) return MT_KERNEL_SIMT;
+  if (d->kernel == MT_KERNEL_SIMT || fp8_cache(d)) return MT_KERNEL_SIMT;
   if (d->kernel == MT_KERNEL_TC) return MT_KERNEL_TC;
   if (d->dtype == MT_F32) return MT_KERNEL_SIMT;
   return tc_supported(d->head_dim, d->num_q_heads / d->num_kv_heads) ? MT_KERNEL_TC : MT_KERNEL_SIMT;
@@ -105,6 +110,12 @@ int check_desc(const mt_attn_desc* d) {
       (d->dtype == MT_F32 || !tc_supported(d->head_dim, d->num_q_heads / d->num_kv_heads)))
     return MT_ERR_UNSUPPORTED;
   if (!(d->sm_scale >= 0.f) || std::isinf(d->sm_scale)) return MT_ERR_INVALID_ARG;
+  if (d->cache_dtype != 0 && d->cache_dtype != MT_E4M3) return MT_ERR_UNSUPPORTED;
+  if (fp8_cache(d)) {
+    if (!(d->k_scale > 0.f) || std::isinf(d->k_scale) || !(d->v_scale > 0.f) || std::isinf(d->v_scale))
+      return MT_ERR_INVALID_ARG;
+    if (d->kernel == MT_KERNEL_TC) return MT_ERR_UNSUPPORTED;
+  }
   return MT_OK;
 }
 
@@ -207,6 +218,7 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   pp.block_tables = block_tables; pp.seq_lens = seq_lens;
   pp.tree_parents = tree_parents; pp.tree_depths = tree_depths;
   pp.rope = rope->table; pp.status = status;
+  pp.cache_fp8 = fp8_cache(d); pp.k_scale = d->k_scale; pp.v_scale = d->v_scale;
   pp.anc = reinterpret_cast<unsigned long long*>(ws + w.anc);
   pp.tile_pfx = reinterpret_cast<int*>(ws + w.pfx);
   Sched sched{};
@@ -240,7 +252,7 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   const bool prof = g_prof_n < g_prof_cap;
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);
   if (kernel == MT_KERNEL_SIMT) {
-    st = cuda_status(launch_attn_simt(ap, d->dtype, stream));
+    st = cuda_status(launch_attn_simt(ap, Fp8Cache{fp8_cache(d), d->k_scale, d->v_scale}, d->dtype, stream));
   } else {
     alignas(64) unsigned char tmap_k[128], tmap_v[128], tmap_q[128];
     if (make_cache_tmap(tmap_k, k_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
@@ -308,7 +320,7 @@ int mt_kv_commit(const mt_attn_desc* d, int max_depth, const int32_t* accept_pat
   c.P = d->page_size; c.max_blocks = d->max_blocks_per_seq; c.num_pages = d->num_pages;
   c.max_depth = max_depth;
   c.rel_width = (d->tree_size + 2 * d->page_size - 2) / d->page_size;
-  c.elem_bytes = elem_bytes(d->dtype);
+  c.elem_bytes = cache_elem_bytes(d);
   c.accept_path = accept_path; c.accept_len = accept_len;
   c.k_cache = k_cache; c.v_cache = v_cache; c.block_tables = block_tables;
   c.seq_lens = seq_lens; c.released = released_pages;
@@ -349,7 +361,7 @@ int mt_tree_accept_commit(const mt_attn_desc* d, int vocab, int max_depth, mt_dt
   c.P = d->page_size; c.max_blocks = d->max_blocks_per_seq; c.num_pages = d->num_pages;
   c.max_depth = max_depth;
   c.rel_width = (tree_size + 2 * d->page_size - 2) / d->page_size;
-  c.elem_bytes = elem_bytes(d->dtype);
+  c.elem_bytes = cache_elem_bytes(d);
   c.accept_path = accept_path; c.accept_len = accept_len;
   c.k_cache = k_cache; c.v_cache = v_cache; c.block_tables = block_tables;
   c.seq_lens = seq_lens; c.released = released_pages;

@@ -1,7 +1,7 @@
 // SIMT (CUDA-core) tree attention over the paged KV cache.
 //
-// The fp32 path, and for fp16/bf16 an independent second implementation that
-// the tests hold against the tensor-core kernel.  Per piece of the schedule
+// The fp32 path, the FP8 (E4M3) cache path, and for fp16/bf16 an independent
+// second implementation that the tests hold against the tensor-core kernel.  Per piece of the schedule
 // (see common.cuh) a CTA takes one 64-row group of (node, head) query rows of
 // one (sequence, KV head) and streams that piece's 64-slot key tiles through
 // shared memory: scores, online softmax in base 2, then P.V, all in fp32.
@@ -9,6 +9,8 @@
 // Visibility of key slot k to the row of node i (the Medusa tree mask, vLLM
 // issue 1171): k < L_b (a committed prefix token), or L_b <= k < L_b + T and
 // bit (k - L_b) of anc[i] is set (a tree ancestor of i, or i itself).
+#include <cuda_fp8.h>
+
 #include "kernels.cuh"
 
 namespace mt {
@@ -47,8 +49,41 @@ __device__ __forceinline__ void load_kv_tile(const T* __restrict__ cache, float*
   }
 }
 
+// The same tile from an FP8 cache: 16 E4M3 codes per 16-byte load, each
+// decoded exactly (through fp16, which holds every E4M3 value) and scaled.
+template <int D>
+__device__ __forceinline__ void load_kv_tile_e4m3(const uint8_t* __restrict__ cache, float* dst, int b,
+                                                  int kvh, int k0, int nkeys, float scale, const AttnParams& a) {
+  constexpr int LD = D + 1;
+  constexpr int EPV = 16;
+  constexpr int VPR = D / EPV;
+  for (int v = threadIdx.x; v < kTileKeys * VPR; v += blockDim.x) {
+    const int key = v / VPR, part = v % VPR;
+    const int slot = k0 + key;
+    float vals[EPV];
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) vals[e] = 0.f;
+    if (slot < nkeys) {
+      const int page = a.block_tables[(size_t)b * a.max_blocks + slot / a.P];
+      if (page >= 0 && page < a.num_pages) {
+        const uint8_t* src = cache + (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * D + part * EPV;
+        uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+        uint8_t codes[EPV];
+        memcpy(codes, &raw, 16);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+          vals[e] = __half2float(__half(__nv_cvt_fp8_to_halfraw(codes[e], __NV_E4M3))) * scale;
+      } else {
+        set_status(a.status, kStPages);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) dst[key * LD + part * EPV + e] = vals[e];
+  }
+}
+
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(AttnParams a) {
+__global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(AttnParams a, Fp8Cache f8) {
   constexpr int R = kSimtRows;
   constexpr int LD = D + 1;
   constexpr int PLD = kTileKeys + 1;
@@ -100,7 +135,10 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
 
     for (int jt = pc.tile_begin; jt < pc.tile_end; ++jt) {
       const int k0 = jt * kTileKeys;
-      load_kv_tile<T, D>(kc, KV, b, kvh, k0, nkeys, a);
+      if (f8.on)
+        load_kv_tile_e4m3<D>(static_cast<const uint8_t*>(a.k_cache), KV, b, kvh, k0, nkeys, f8.k_scale, a);
+      else
+        load_kv_tile<T, D>(kc, KV, b, kvh, k0, nkeys, a);
       __syncthreads();
       float s[4][4];
 #pragma unroll
@@ -151,7 +189,10 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
         for (int c = 0; c < NC; ++c) o[i][c] *= alpha;
       }
       __syncthreads();
-      load_kv_tile<T, D>(vc, KV, b, kvh, k0, nkeys, a);
+      if (f8.on)
+        load_kv_tile_e4m3<D>(static_cast<const uint8_t*>(a.v_cache), KV, b, kvh, k0, nkeys, f8.v_scale, a);
+      else
+        load_kv_tile<T, D>(vc, KV, b, kvh, k0, nkeys, a);
       __syncthreads();
 #pragma unroll 4
       for (int k = 0; k < kTileKeys; ++k) {
@@ -195,29 +236,29 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
 }
 
 template <typename T, int D>
-cudaError_t launch_simt_t(const AttnParams& a, cudaStream_t stream) {
+cudaError_t launch_simt_t(const AttnParams& a, const Fp8Cache& f8, cudaStream_t stream) {
   constexpr int LD = D + 1;
   const size_t smem = sizeof(float) * (size_t)(kSimtRows * LD + kTileKeys * LD + kSimtRows * (kTileKeys + 1));
   cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(attn_simt_kernel<T, D>, dim3(a.sched.G), dim3(kThreads), smem, stream, a);
+  return launch_pdl(attn_simt_kernel<T, D>, dim3(a.sched.G), dim3(kThreads), smem, stream, a, f8);
 }
 
 }  // namespace
 
-cudaError_t launch_attn_simt(const AttnParams& a, int dtype, cudaStream_t stream) {
+cudaError_t launch_attn_simt(const AttnParams& a, const Fp8Cache& f8, int dtype, cudaStream_t stream) {
   if (a.D == 64) {
     switch (dtype) {
-      case 0: return launch_simt_t<float, 64>(a, stream);
-      case 1: return launch_simt_t<__half, 64>(a, stream);
-      default: return launch_simt_t<__nv_bfloat16, 64>(a, stream);
+      case 0: return launch_simt_t<float, 64>(a, f8, stream);
+      case 1: return launch_simt_t<__half, 64>(a, f8, stream);
+      default: return launch_simt_t<__nv_bfloat16, 64>(a, f8, stream);
     }
   }
   switch (dtype) {
-    case 0: return launch_simt_t<float, 128>(a, stream);
-    case 1: return launch_simt_t<__half, 128>(a, stream);
-    default: return launch_simt_t<__nv_bfloat16, 128>(a, stream);
+    case 0: return launch_simt_t<float, 128>(a, f8, stream);
+    case 1: return launch_simt_t<__half, 128>(a, f8, stream);
+    default: return launch_simt_t<__nv_bfloat16, 128>(a, f8, stream);
   }
 }
 

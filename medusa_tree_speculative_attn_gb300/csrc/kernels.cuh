@@ -53,6 +53,8 @@ struct PrepParams {
   int* tile_pfx;            // [B + 1]
   Sched sched;              // the attention kernel's schedule (tile_pfx unused)
   int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs], or null
+  int cache_fp8;            // the caches hold FP8 E4M3 codes of value / scale
+  float k_scale, v_scale;
 };
 
 // Candidate tree tokens from the Medusa heads (cand.cu).
@@ -99,7 +101,13 @@ constexpr int kTcRows = 256;
 constexpr int kTcCtasPerSm = 1;
 
 cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream);
-cudaError_t launch_attn_simt(const AttnParams& a, int dtype, cudaStream_t stream);
+// An FP8 (E4M3) KV cache: codes of value / scale, read by the CUDA-core kernel only.
+struct Fp8Cache {
+  int on;
+  float k_scale, v_scale;
+};
+
+cudaError_t launch_attn_simt(const AttnParams& a, const Fp8Cache& f8, int dtype, cudaStream_t stream);
 // Encode TMA descriptors (128 bytes, 64-byte aligned): a paged cache, and the
 // rotated queries [B*T][Hq][D] in boxes of 128 rows (128/g nodes x g heads).
 cudaError_t make_cache_tmap(void* map_out, const void* base, int dtype, int num_pages, int Hkv,

@@ -10,6 +10,8 @@
 // rotated at position L_b + depth[i] (TensorRT-LLM issue 1946, position
 // offsets for Medusa tokens); keys land at logical slot L_b + i, queries in a
 // [B][T][Hq][D] workspace array read by the attention kernels.
+#include <cuda_fp8.h>
+
 #include "kernels.cuh"
 
 namespace mt {
@@ -45,6 +47,20 @@ template <> struct Vec8<__nv_bfloat16> {
     *reinterpret_cast<uint4*>(p) = v;
   }
 };
+
+// Eight act-dtype values into an FP8 cache: the E4M3 codes of value / scale
+// (fp32 division, nearest-even, saturated to +-448), one 8-byte store.
+template <typename T>
+__device__ __forceinline__ void store_e4m3x8(uint8_t* p, const typename Vec8<T>::type& v, float scale) {
+  T x[8];
+  memcpy(x, &v, sizeof(x));
+  uint8_t c[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) c[e] = __nv_cvt_float_to_fp8(Act<T>::to_f(x[e]) / scale, __NV_SATFINITE, __NV_E4M3);
+  uint2 w;
+  memcpy(&w, c, 8);
+  *reinterpret_cast<uint2*>(p) = w;
+}
 
 // Exclusive scan of n values with one block; returns the total.
 __device__ int block_exclusive_scan(int* data, int n, int* warp_sums) {
@@ -275,7 +291,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
       if (k == 0) set_status(a.status, L < 0 ? kStPages : kStTree);
       continue;
     }
-    T* dst;
+    T* dst = nullptr;        // act-dtype destination of the rotated row
+    uint8_t* dst8 = nullptr;  // FP8 cache destination of a rotated key
     if (is_q) {
       dst = static_cast<T*>(a.q_rot) + (size_t)row * a.D;
     } else {
@@ -287,11 +304,19 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
         continue;
       }
       const size_t off = (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * a.D;
-      dst = static_cast<T*>(a.k_cache) + off;
-      // raw value: this lane's two 8-element chunks
-      T* vc = static_cast<T*>(a.v_cache) + off;
-      Vec8<T>::store(vc + 8 * k, vlo);
-      Vec8<T>::store(vc + half + 8 * k, vhi);
+      if (a.cache_fp8) {
+        // FP8 cache: the codes of the raw value and (below) of the rotated key
+        dst8 = static_cast<uint8_t*>(a.k_cache) + off;
+        uint8_t* vc8 = static_cast<uint8_t*>(a.v_cache) + off;
+        store_e4m3x8<T>(vc8 + 8 * k, vlo, a.v_scale);
+        store_e4m3x8<T>(vc8 + half + 8 * k, vhi, a.v_scale);
+      } else {
+        dst = static_cast<T*>(a.k_cache) + off;
+        // raw value: this lane's two 8-element chunks
+        T* vc = static_cast<T*>(a.v_cache) + off;
+        Vec8<T>::store(vc + 8 * k, vlo);
+        Vec8<T>::store(vc + half + 8 * k, vhi);
+      }
     }
     const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * half + 8 * k);
     T lo[8], hi[8], olo[8], ohi[8];
@@ -311,8 +336,13 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
     typename Vec8<T>::type wl, wh;
     memcpy(&wl, olo, sizeof(olo));
     memcpy(&wh, ohi, sizeof(ohi));
-    Vec8<T>::store(dst + 8 * k, wl);
-    Vec8<T>::store(dst + half + 8 * k, wh);
+    if (dst8) {
+      store_e4m3x8<T>(dst8 + 8 * k, wl, a.k_scale);
+      store_e4m3x8<T>(dst8 + half + 8 * k, wh, a.k_scale);
+    } else {
+      Vec8<T>::store(dst + 8 * k, wl);
+      Vec8<T>::store(dst + half + 8 * k, wh);
+    }
   }
 }
 

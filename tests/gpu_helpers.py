@@ -25,6 +25,8 @@ def to_host(t: torch.Tensor) -> np.ndarray:
     t = t.detach().cpu()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8).numpy()
     return t.numpy()
 
 
@@ -63,6 +65,7 @@ class Step:
         self.rope = mt.Rope(w["rope_base"], w["head_dim"], int(np.max(_host(w, "seq_lens"))) + w["T"] + 1)
         self.desc = mt.make_desc(d["q"], d["k_cache"], d["block_tables"], num_splits, kernel)
         self.kernel, self.num_splits = kernel, num_splits
+        self.k_scale = self.v_scale = 1.0   # FP8 caches only
         self.ws = mt.alloc_attn_workspace(self.desc, dev)
         self.out = torch.empty_like(d["q"])
         B, T = w["B"], w["T"]
@@ -79,7 +82,8 @@ class Step:
         mt.tree_attn_paged(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["seq_lens"],
                            d["tree_parents"], d["tree_depths"], self.out, k_new=d["k_new"],
                            v_new=d["v_new"], rope=self.rope, workspace=self.ws,
-                           num_splits=self.num_splits, kernel=self.kernel)
+                           num_splits=self.num_splits, kernel=self.kernel, k_scale=self.k_scale,
+                           v_scale=self.v_scale)
 
     def accept(self):
         d = self.d

@@ -50,7 +50,8 @@ def test_status_strings_and_version(lib):
 def _desc(**kw):
     import medusa_tree_speculative_attn_gb300 as mt
     base = dict(batch=2, tree_size=8, num_q_heads=8, num_kv_heads=2, head_dim=128, page_size=16,
-                max_blocks_per_seq=8, num_pages=32, num_splits=0, dtype=2, sm_scale=0.0, kernel=0)
+                max_blocks_per_seq=8, num_pages=32, num_splits=0, dtype=2, sm_scale=0.0, kernel=0,
+                cache_dtype=0, k_scale=1.0, v_scale=1.0)
     base.update(kw)
     return mt.AttnDesc(**base)
 
@@ -60,6 +61,11 @@ def _desc(**kw):
     (dict(page_size=32), -2), (dict(num_q_heads=6, num_kv_heads=4), -1), (dict(batch=0), -1),
     (dict(dtype=7), -2), (dict(kernel=9), -1), (dict(kernel=2, dtype=0), -2),
     (dict(num_splits=-1), -1), (dict(sm_scale=float("nan")), -1),
+    # FP8 cache: E4M3 only, as a cache type only, positive finite scales, not on tensor cores
+    (dict(dtype=3), -2), (dict(cache_dtype=5), -2), (dict(cache_dtype=1), -2),
+    (dict(cache_dtype=3, k_scale=0.0), -1), (dict(cache_dtype=3, v_scale=-1.0), -1),
+    (dict(cache_dtype=3, k_scale=float("nan")), -1), (dict(cache_dtype=3, v_scale=float("inf")), -1),
+    (dict(cache_dtype=3, kernel=2), -2),
 ])
 def test_attn_rejects_bad_descriptors(lib, kw, code):
     d = _desc(**kw)
