@@ -63,6 +63,8 @@ def _load():
             lib.or_tree_scatter.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32,
                                             P, P, P, P, P, P]
             lib.or_accept_greedy.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P]
+            lib.or_accept_typical.argtypes = [i32, i32, i32, i32, i32, P, P, P, dbl, dbl, dbl,
+                                              P, P, P, P, P, P]
             lib.or_tree_candidates.argtypes = [i32, i32, i32, i32, i32, P, P, P, P]
             lib.or_kv_commit.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32,
                                          P, P, P, P, P, P, P, i32]
@@ -279,6 +281,27 @@ def accept_greedy(tokens, logits: np.ndarray, logits_dtype: str, parents, max_de
                                   _ptr(nxt))
     _check(st, "accept_greedy")
     return am, alen, path, nxt
+
+
+def accept_typical(tokens, logits: np.ndarray, logits_dtype: str, parents, max_depth: int,
+                   temperature: float, epsilon: float, delta: float):
+    """Typical acceptance (see or_accept_typical for the reading).  Returns a dict:
+    node_accept [B,T] int32 (each node's own test), prob and thr [B,T] float64
+    (q[token] and min(epsilon, delta*exp(-H)) of the parent's row), accept_len [B],
+    accept_path [B,max_depth+1], next_token [B], status."""
+    tokens = _i32(tokens)
+    parents = _i32(parents)
+    B, T = tokens.shape
+    V = logits.shape[-1]
+    logits = _act(logits, logits_dtype)
+    r = dict(node_accept=np.zeros((B, T), np.int32), prob=np.zeros((B, T)), thr=np.zeros((B, T)),
+             accept_len=np.zeros(B, np.int32), accept_path=np.full((B, max_depth + 1), -1, np.int32),
+             next_token=np.zeros(B, np.int32))
+    r["status"] = _load().or_accept_typical(
+        DTYPES[logits_dtype], B, T, V, max_depth, _ptr(tokens), _ptr(logits), _ptr(parents),
+        float(temperature), float(epsilon), float(delta), _ptr(r["node_accept"]), _ptr(r["prob"]),
+        _ptr(r["thr"]), _ptr(r["accept_len"]), _ptr(r["accept_path"]), _ptr(r["next_token"]))
+    return r
 
 
 def tree_candidates(root_logits: np.ndarray, head_logits: np.ndarray, logits_dtype: str, parents):

@@ -22,7 +22,9 @@
  *    answer by rakib-hasan: a position-offset tensor makes RoPE rotate each
  *    Medusa token at its own position (prefix length + tree depth here).
  *  - lmdeploy PR 1231 "[WIP] support Medusa": greedy acceptance at LM-head
- *    temperature 0 (`evaluate_posterior`), verified with a 64-choice tree.
+ *    temperature 0 (`evaluate_posterior`), verified with a 64-choice tree; a
+ *    "typical acceptance scheme" is named there but not defined (the reading
+ *    taken is stated at or_accept_typical).
  *
  * Readings the pages leave open (the node-0 root at position prefix_len,
  * self-visibility, NeoX half-split RoPE pairing, 1/sqrt(D) scale, lowest index
@@ -537,6 +539,97 @@ int or_accept_greedy(int dt, int B, int T, int V, int max_depth, const int32_t* 
     for (int a = end; a >= 0; a = par[a]) path[depth[a]] = a;
     next_token[b] = am[end];
   }
+  return status;
+}
+
+/* Typical acceptance.  The pages name a "typical acceptance scheme" beside
+ * tree attention as the part of Medusa that inference frameworks lack
+ * (lmdeploy PR 1231, comment on adopting Medusa heads) but never define it.
+ * Reading taken, from the Medusa paper's typical-acceptance rule (Cai et al.,
+ * "Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding
+ * Heads", 2024), restated: a tree node i > 0 passes when the target model's
+ * tempered distribution at its parent,
+ *     q_v = exp(x_v / tau) / sum_u exp(x_u / tau)   (x = the parent's logits row),
+ * gives its token more than
+ *     thr = min(epsilon, delta * exp(-H)),   H = -sum_v q_v ln q_v   (nats),
+ * i.e. q[token_i] > thr (a token outside [0, V) has q = 0 and fails).  The
+ * root always passes.  The accepted path is then chosen exactly as in greedy
+ * acceptance (every node on the root path passes; deepest end, lowest index
+ * among equals), and next_token is the end row's argmax (the bonus token at
+ * temperature 0: no random draw).
+ * Outputs per node: node_accept (the node's own test, 1 at the root),
+ * prob = q[token_i] and thr of its parent's row (1 and 0 at the root). */
+int or_accept_typical(int dt, int B, int T, int V, int max_depth, const int32_t* tokens,
+                      const void* logits, const int32_t* parents, double tau, double epsilon,
+                      double delta, int32_t* node_accept, double* prob, double* thr,
+                      int32_t* accept_len, int32_t* accept_path, int32_t* next_token) {
+  if (B < 0 || T < 1 || T > 64 || V < 1 || max_depth < 0) return OR_ERR_ARG;
+  if (!(tau > 0.0) || !(epsilon > 0.0) || !(delta > 0.0) || isinf(tau) || isinf(epsilon) ||
+      isinf(delta))
+    return OR_ERR_ARG;
+  int status = OR_OK;
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!q) return OR_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* par = parents + (size_t)b * T;
+    const int32_t* tok = tokens + (size_t)b * T;
+    if (check_tree(T, par, NULL)) { status = OR_ERR_TREE; continue; }
+    int depth[64];
+    depth[0] = 0;
+    for (int i = 1; i < T; ++i) depth[i] = depth[par[i]] + 1;
+    int too_deep = 0;
+    for (int i = 0; i < T; ++i) if (depth[i] > max_depth) too_deep = 1;
+    if (too_deep) { status = OR_ERR_TREE; continue; }
+    /* each node's own test, under its parent's tempered distribution */
+    int pass[64];
+    pass[0] = 1;
+    node_accept[(size_t)b * T] = 1;
+    prob[(size_t)b * T] = 1.0;
+    thr[(size_t)b * T] = 0.0;
+    for (int i = 1; i < T; ++i) {
+      const size_t row = ((size_t)b * T + par[i]) * (size_t)V;
+      double m = -INFINITY;
+      for (int v = 0; v < V; ++v) {
+        const double xv = load_act(dt, logits, row + v) / tau;
+        if (xv > m) m = xv;
+      }
+      double z = 0.0;
+      for (int v = 0; v < V; ++v) {
+        q[v] = exp(load_act(dt, logits, row + v) / tau - m);
+        z += q[v];
+      }
+      double h = 0.0;
+      for (int v = 0; v < V; ++v) {
+        q[v] /= z;
+        if (q[v] > 0.0) h -= q[v] * log(q[v]);
+      }
+      const double t = fmin(epsilon, delta * exp(-h));
+      const double pt = (tok[i] >= 0 && tok[i] < V) ? q[tok[i]] : 0.0;
+      pass[i] = pt > t;
+      node_accept[(size_t)b * T + i] = pass[i];
+      prob[(size_t)b * T + i] = pt;
+      thr[(size_t)b * T + i] = t;
+    }
+    int acc[64];
+    acc[0] = 1;
+    for (int i = 1; i < T; ++i) acc[i] = acc[par[i]] && pass[i];
+    int end = 0;
+    for (int i = 1; i < T; ++i)
+      if (acc[i] && depth[i] > depth[end]) end = i;   /* strict: lowest index wins ties */
+    accept_len[b] = depth[end];
+    int32_t* path = accept_path + (size_t)b * (max_depth + 1);
+    for (int d = 0; d <= max_depth; ++d) path[d] = -1;
+    for (int a = end; a >= 0; a = par[a]) path[depth[a]] = a;
+    const size_t erow = ((size_t)b * T + end) * (size_t)V;
+    double best = load_act(dt, logits, erow);
+    int best_v = 0;
+    for (int v = 1; v < V; ++v) {
+      const double x = load_act(dt, logits, erow + v);
+      if (x > best) { best = x; best_v = v; }
+    }
+    next_token[b] = best_v;
+  }
+  free(q);
   return status;
 }
 
