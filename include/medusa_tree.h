@@ -16,6 +16,9 @@
  *                         scratch pages past the new length are released;
  *
  * or in two, with mt_tree_accept_commit doing the last two in one launch.
+ * mt_tree_accept_typical replaces greedy acceptance by typical acceptance
+ * (a tempered-probability threshold), and mt_tree_candidates builds the tree's
+ * tokens from the Medusa heads before the step.
  *
  * What the pages fix, per call:
  *  - vLLM issue 1171 "[Discussion] Will vLLM consider using Speculative
@@ -206,8 +209,8 @@ int mt_tree_attn_paged_noalloc(const mt_attn_desc* desc, const void* q, const vo
  *   tree_tokens int32 [B][T]; target_logits [B][T][V] in logits_dtype (no NaN);
  *   tree_parents int32 [B][T]; every depth must be <= max_depth.
  *   workspace: mt_tree_accept_workspace_size(B, T) bytes, zero-filled before
- *   first use (status word and per-sequence arrival counters, which every call
- *   leaves at zero). */
+ *   first use (status word, per-sequence arrival counters, which every call
+ *   leaves at zero, and per-node scratch for typical acceptance). */
 size_t mt_tree_accept_workspace_size(int batch, int tree_size);
 int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
                           mt_dtype logits_dtype, const int32_t* tree_tokens,
@@ -215,6 +218,33 @@ int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
                           int32_t* argmax_out, int32_t* accept_len, int32_t* accept_path,
                           int32_t* next_token, void* workspace, size_t ws_bytes,
                           cudaStream_t stream);
+
+/* ---- Typical acceptance ---------------------------------------------------
+ * The "typical acceptance scheme" that lmdeploy PR 1231 ("[WIP] support
+ * Medusa") names beside tree attention; the pages do not define it, and the
+ * rule taken is the Medusa paper's (Cai et al. 2024, typical acceptance).
+ * Per sequence b, with x the logits row of a node and tau = temperature:
+ *   q_v = exp(x_v / tau) / sum_u exp(x_u / tau), H = -sum_v q_v ln q_v;
+ *   node i > 0 passes when q[tree_tokens[b][i]] > min(epsilon, delta * exp(-H))
+ *     under its parent's row (a token outside [0, vocab) fails); the root
+ *     passes; node_accept[b][i] = 1 when node i passes (its own test);
+ *   accept_len, accept_path: as in mt_tree_accept_greedy with "accepted" =
+ *     every node on the root path passes;
+ *   next_token[b] = argmax of the end node's row (lowest index among equal
+ *     maxima): the bonus token at temperature 0, no random draw.
+ * Computed in fp32: the device sums the row in an order of its own, so a
+ * node whose q[token] lies within a relative 1e-5 or so of its threshold may
+ * fall either way.  temperature, epsilon, delta: positive and finite
+ * (MT_ERR_INVALID_ARG otherwise; also when log2(e) / temperature overflows).
+ * Logits: finite, and finite after scaling by log2(e) / temperature.
+ * Layouts, max_depth and the workspace as for mt_tree_accept_greedy (the
+ * same mt_tree_accept_workspace_size); node_accept int32 [B][T]. */
+int mt_tree_accept_typical(int batch, int tree_size, int vocab, int max_depth,
+                           mt_dtype logits_dtype, const int32_t* tree_tokens,
+                           const void* target_logits, const int32_t* tree_parents,
+                           float temperature, float epsilon, float delta, int32_t* node_accept,
+                           int32_t* accept_len, int32_t* accept_path, int32_t* next_token,
+                           void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /* ---- KV commit --------------------------------------------------------------
  * For each sequence b, with L = accept_len[b] and len = seq_lens[b]:

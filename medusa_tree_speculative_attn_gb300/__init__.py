@@ -70,6 +70,8 @@ def _load():
         lib.mt_tree_accept_workspace_size.argtypes = [I, I]
         lib.mt_tree_accept_workspace_size.restype = Z
         lib.mt_tree_accept_greedy.argtypes = [I, I, I, I, I] + [P] * 8 + [Z, P]
+        lib.mt_tree_accept_typical.argtypes = ([I, I, I, I, I] + [P] * 3 + [ctypes.c_float] * 3 +
+                                               [P] * 5 + [Z, P])
         lib.mt_kv_commit.argtypes = [D, I] + [P] * 8 + [P]
         lib.mt_tree_accept_commit.argtypes = [D, I, I, I] + [P] * 12 + [P, Z, P]
         lib.mt_tree_candidates.argtypes = [I, I, I, I, I] + [P] * 5 + [P]
@@ -228,6 +230,35 @@ def tree_accept_greedy(tree_tokens, target_logits, tree_parents, accept_len, acc
                                        _ptr(next_token), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "mt_tree_accept_greedy")
+    return accept_len, accept_path
+
+
+def tree_accept_typical(tree_tokens, target_logits, tree_parents, accept_len, accept_path, *,
+                        node_accept, next_token, workspace: torch.Tensor, temperature: float,
+                        epsilon: float, delta: float, max_depth: Optional[int] = None, stream=None):
+    """Typical acceptance: node i passes when its token's probability under its
+    parent's tempered row exceeds min(epsilon, delta * exp(-entropy)); fills
+    node_accept, accept_len, accept_path, next_token (the end row's argmax)."""
+    _need(tree_tokens, "tree_tokens", torch.int32, 2)
+    _need(tree_parents, "tree_parents", torch.int32, 2)
+    _need(target_logits, "target_logits", None, 3)
+    for name, t in (("accept_len", accept_len), ("next_token", next_token)):
+        _need(t, name, torch.int32, 1)
+    _need(accept_path, "accept_path", torch.int32, 2)
+    _need(node_accept, "node_accept", torch.int32, 2)
+    B, T = tree_tokens.shape
+    V = target_logits.shape[2]
+    if max_depth is None:
+        max_depth = accept_path.shape[1] - 1
+    if accept_path.shape[1] != max_depth + 1:
+        raise ValueError("accept_path must have max_depth + 1 columns")
+    st = _load().mt_tree_accept_typical(B, T, V, int(max_depth), _DTYPES[target_logits.dtype],
+                                        _ptr(tree_tokens), _ptr(target_logits), _ptr(tree_parents),
+                                        float(temperature), float(epsilon), float(delta),
+                                        _ptr(node_accept), _ptr(accept_len), _ptr(accept_path),
+                                        _ptr(next_token), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "mt_tree_accept_typical")
     return accept_len, accept_path
 
 

@@ -11,6 +11,12 @@
 //   end = the deepest accepted node (lowest index among equals),
 // writes accept_len, the padded root-to-end path and next_token, and, in the
 // fused form, commits the sequence's K/V (commit_seq.cuh) right away.
+//
+// Typical acceptance (the scheme lmdeploy PR 1231 names beside tree attention;
+// the rule of the Medusa paper) has the same shape: each row's CTA streams its
+// logits once for the argmax and the tempered distribution's statistics, and
+// node i > 0 passes when its token's probability under its parent's row is
+// above min(epsilon, delta * exp(-entropy)).
 #include "commit_seq.cuh"
 
 namespace mt {
@@ -88,6 +94,12 @@ struct SeqPrefetch {
   }
 };
 
+struct GreedyTest {
+  __device__ __forceinline__ bool operator()(const FinishSmem& sm, int i, int p) const {
+    return sm.tok[i] != sm.am[p];
+  }
+};
+
 // Greedy path of sequence b by one warp, every step in parallel over the nodes
 // (lane l owns nodes l and l + 32):
 //   ancestors and depths by pointer jumping (six rounds close any depth < 64);
@@ -95,12 +107,14 @@ struct SeqPrefetch {
 //   node i is accepted when every node on its root path matches;
 //   end = the accepted node of largest depth, the lowest index among equals.
 // The argmax values were written by other CTAs: read through L2.  Parents and
-// tokens come from shared memory (SeqPrefetch).
-__device__ void select_path(const AcceptParams& a, int b, FinishSmem& sm) {
+// tokens come from shared memory (SeqPrefetch).  fails(sm, i, p) says whether
+// node i > 0 with the valid parent p fails its own test (greedy: tokens[i] !=
+// argmax[p]).
+template <class Fails = GreedyTest>
+__device__ void select_path(const AcceptParams& a, int b, FinishSmem& sm, Fails fails = Fails()) {
   const int lane = threadIdx.x & 31;
   const int T = a.T;
   const int* par = sm.par;
-  const int* tok = sm.tok;
   const int* am = a.argmax_out + (size_t)b * T;
   bool good = true;
   for (int i = lane; i < T; i += 32) {
@@ -143,11 +157,11 @@ __device__ void select_path(const AcceptParams& a, int b, FinishSmem& sm) {
     const int i0 = lane, i1 = lane + 32;
     if (i0 < T && i0 > 0) {
       const int p = par[i0];
-      mis0 = !(p >= 0 && p < i0) || tok[i0] != sm.am[p];
+      mis0 = !(p >= 0 && p < i0) || fails(sm, i0, p);
     }
     if (i1 < T) {
       const int p = par[i1];
-      mis1 = !(p >= 0 && p < i1) || tok[i1] != sm.am[p];
+      mis1 = !(p >= 0 && p < i1) || fails(sm, i1, p);
     }
   }
   const unsigned long long mis = (unsigned long long)__ballot_sync(0xffffffffu, mis0) |
@@ -315,6 +329,206 @@ __global__ void __launch_bounds__(kThreads) argmax_scalar_kernel(AcceptParams a,
   finish_row<kCommit>(a, c, row, ix, sm, stage, stage_vecs);
 }
 
+// ---- typical acceptance ----------------------------------------------------
+//
+// Per row, in base-2 units y = logit * k with k = log2(e) / temperature:
+//   m = max y,  Z = sum 2^(y - m),  S = sum 2^(y - m) (y - m),
+// so that the tempered distribution is q_v = 2^(y_v - m) / Z and its entropy
+// in bits is H = log2 Z - S / Z (H ln 2 in nats, and exp(-H ln 2) = 2^-H).
+// Each thread keeps a running (m, Z, S), moved to a larger m by scaling
+// (Z, S) -> (c Z, c (S + (m_old - m) Z)), c = 2^(m_old - m).
+struct RowStats {
+  float m = -INFINITY, z = 0.f, s = 0.f;
+  __device__ __forceinline__ void rebase(float nm) {  // nm >= m
+    if (z > 0.f) {
+      const float d = m - nm;
+      const float c = exp2f(d);
+      s = c * (s + d * z);
+      z *= c;
+    }
+    m = nm;
+  }
+  __device__ __forceinline__ void add(float y) {  // y <= m
+    const float t = y - m;
+    const float e = exp2f(t);
+    z += e;
+    s += e > 0.f ? e * t : 0.f;
+  }
+  __device__ __forceinline__ void merge(RowStats o) {
+    const float nm = fmaxf(m, o.m);
+    if (nm == -INFINITY) return;
+    rebase(nm);
+    o.rebase(nm);
+    z += o.z;
+    s += o.s;
+  }
+  __device__ __forceinline__ void warp_merge() {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      RowStats o;
+      o.m = __shfl_xor_sync(0xffffffffu, m, off);
+      o.z = __shfl_xor_sync(0xffffffffu, z, off);
+      o.s = __shfl_xor_sync(0xffffffffu, s, off);
+      merge(o);
+    }
+  }
+};
+
+// A node's test, read by the warp that selects the path (typ_ok, filled first).
+struct TypicalTest {
+  const int* ok;
+  __device__ __forceinline__ bool operator()(const FinishSmem&, int i, int) const { return ok[i] == 0; }
+};
+
+// The typical row pass's end, for every thread of the row's CTA: thread 0
+// holds the row's argmax ix and statistics st.  Publish both; the CTA that
+// completes the sequence fills each node's test (one warp, two nodes a lane:
+// the token's logit is read again from its parent's row), writes node_accept
+// and selects the path.
+template <typename T>
+__device__ void finish_typical(const AcceptParams& a, const TypicalParams& t, int row, int ix, RowStats st,
+                               FinishSmem& sm, int* typ_ok) {
+  const int b = row / a.T;
+  if (threadIdx.x == 0) {
+    const float h = log2f(st.z) - st.s / st.z;  // entropy in bits
+    const float thr = fminf(t.epsilon, t.delta * exp2f(-h));
+    t.stats[row] = make_float4(st.m, st.z, thr, 0.f);
+    a.argmax_out[row] = ix;
+    __threadfence();  // the row's results are visible before the arrival is
+    sm.last = atomicAdd(&a.counters[b], 1u) == (unsigned)(a.T - 1);
+  }
+  __syncthreads();
+  if (!sm.last) return;
+  __threadfence();  // every other row's results are visible past this point
+  if (threadIdx.x == 0) a.counters[b] = 0;
+  if (threadIdx.x >= 32) return;
+  const T* lg = static_cast<const T*>(a.logits);
+  for (int i = threadIdx.x; i < a.T; i += 32) {
+    int ok = 1;
+    if (i > 0) {
+      const int p = sm.par[i], tok = sm.tok[i];
+      ok = 0;
+      if (p >= 0 && p < i && tok >= 0 && tok < a.V) {
+        const size_t prow = (size_t)b * a.T + p;
+        const float4 ps = __ldcg(t.stats + prow);
+        const float y = Act<T>::to_f(lg[prow * a.V + tok]) * t.k;
+        ok = exp2f(y - ps.x) / ps.y > ps.z;
+      }
+    }
+    typ_ok[i] = ok;
+    t.node_accept[(size_t)b * a.T + i] = ok;
+  }
+  __syncwarp();
+  select_path(a, b, sm, TypicalTest{typ_ok});
+}
+
+// Rows of 16-byte vectors (same loads as argmax_rows_kernel), or any row with
+// kVec false (scalar loads).  Every element enters the statistics; the argmax
+// keeps the raw values' order (the lowest index among equal maxima).
+template <typename T, bool kVec>
+__global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptParams a, TypicalParams t) {
+  constexpr int EPV = kVec ? 16 / sizeof(T) : 1;
+  __shared__ float s_v[kRowThreads / 32];
+  __shared__ int s_i[kRowThreads / 32];
+  __shared__ float s_m[kRowThreads / 32], s_z[kRowThreads / 32], s_s[kRowThreads / 32];
+  __shared__ int typ_ok[kMaxTree];
+  __shared__ FinishSmem sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.x;
+  pdl_wait();
+  SeqPrefetch pf;
+  pf.load(a, CommitParams{}, row / a.T, false);
+  const T* base = static_cast<const T*>(a.logits) + (size_t)row * a.V;
+  float best = -INFINITY;
+  int bidx = 0x7fffffff;
+  RowStats st;
+  const int nvec = a.V / EPV;
+  for (int v0 = tid; v0 < nvec; v0 += kRowThreads * kBatch) {
+    // all of the round's loads first (raw vectors, or scalars already widened)
+    uint4 raw[kVec ? kBatch : 1];
+    float xs[kVec ? 1 : kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int v = v0 + j * kRowThreads;
+      if (v < nvec) {
+        if constexpr (kVec) raw[j] = __ldcs(reinterpret_cast<const uint4*>(base) + v);
+        else xs[j] = Act<T>::to_f(base[v]);
+      }
+    }
+    // pass 1: argmax and the round's largest y
+    float bm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int v = v0 + j * kRowThreads;
+      if (v < nvec) {
+        float x[EPV];
+        if constexpr (kVec) {
+          T tmp[EPV];
+          memcpy(tmp, &raw[j], 16);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) x[e] = Act<T>::to_f(tmp[e]);
+        } else {
+          x[0] = xs[j];
+        }
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) {
+          if (x[e] > best || bidx == 0x7fffffff) {  // indices rise within a thread: the first maximum stays
+            best = x[e];
+            bidx = v * EPV + e;
+          }
+          bm = fmaxf(bm, x[e] * t.k);
+        }
+      }
+    }
+    // pass 2: the round's terms, under the running maximum
+    if (bm > st.m) st.rebase(bm);
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      const int v = v0 + j * kRowThreads;
+      if (v < nvec) {
+        if constexpr (kVec) {
+          T tmp[EPV];
+          memcpy(tmp, &raw[j], 16);
+#pragma unroll
+          for (int e = 0; e < EPV; ++e) st.add(Act<T>::to_f(tmp[e]) * t.k);
+        } else {
+          st.add(xs[j] * t.k);
+        }
+      }
+    }
+  }
+  warp_best(best, bidx);
+  st.warp_merge();
+  if (lane == 0) {
+    s_v[warp] = best;
+    s_i[warp] = bidx;
+    s_m[warp] = st.m;
+    s_z[warp] = st.z;
+    s_s[warp] = st.s;
+  }
+  pf.store(a, sm);
+  __syncthreads();
+  float v = lane < kRowThreads / 32 ? s_v[lane] : -INFINITY;
+  int ix = lane < kRowThreads / 32 ? s_i[lane] : 0x7fffffff;
+  RowStats all;
+  if (lane < kRowThreads / 32) {
+    all.m = s_m[lane];
+    all.z = s_z[lane];
+    all.s = s_s[lane];
+  }
+  warp_best(v, ix);  // every warp merges; thread 0's results are used
+  all.warp_merge();
+  finish_typical<T>(a, t, row, ix, all, sm, typ_ok);
+}
+
+template <typename T>
+cudaError_t launch_typical_t(const AcceptParams& a, const TypicalParams& t, cudaStream_t stream) {
+  const int nrows = a.B * a.T;
+  if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0)
+    return launch_pdl(typical_rows_kernel<T, false>, dim3(nrows), dim3(kRowThreads), 0, stream, a, t);
+  return launch_pdl(typical_rows_kernel<T, true>, dim3(nrows), dim3(kRowThreads), 0, stream, a, t);
+}
+
 // The fused kernel's commit stage: every row's CTA carries it, so it stays
 // small enough for 7 CTAs per SM (the serving trees' five path entries of 8
 // bf16 heads of 128 fit in one pass).
@@ -347,6 +561,14 @@ cudaError_t launch_accept(const AcceptParams& a, int dtype, cudaStream_t stream)
 
 cudaError_t launch_accept_commit(const AcceptParams& a, const CommitParams& c, int dtype, cudaStream_t stream) {
   return launch_dtype<true>(a, c, dtype, stream);
+}
+
+cudaError_t launch_accept_typical(const AcceptParams& a, const TypicalParams& t, int dtype, cudaStream_t stream) {
+  switch (dtype) {
+    case 0: return launch_typical_t<float>(a, t, stream);
+    case 1: return launch_typical_t<__half>(a, t, stream);
+    default: return launch_typical_t<__nv_bfloat16>(a, t, stream);
+  }
 }
 
 }  // namespace mt

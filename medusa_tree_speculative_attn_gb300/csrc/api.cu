@@ -270,9 +270,25 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   return cuda_status(launch_combine(ap, d->dtype, stream));
 }
 
+// Acceptance workspace: status word, arrival counters [B], then (typical
+// acceptance) each row's argmax [B*T] int32 and statistics [B*T] float4.
+struct AcceptWs {
+  size_t counters, argmax, stats, total;
+};
+
+AcceptWs accept_ws(int batch, int tree_size) {
+  AcceptWs w;
+  const size_t rows = (size_t)batch * tree_size;
+  w.counters = kAlign;
+  w.argmax = align_up(w.counters + sizeof(unsigned) * (size_t)batch);
+  w.stats = align_up(w.argmax + sizeof(int) * rows);
+  w.total = align_up(w.stats + sizeof(float4) * rows);
+  return w;
+}
+
 size_t mt_tree_accept_workspace_size(int batch, int tree_size) {
   if (batch < 1 || tree_size < 1) return 0;
-  return align_up(kAlign + sizeof(unsigned) * (size_t)batch);
+  return accept_ws(batch, tree_size).total;
 }
 
 int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
@@ -301,6 +317,43 @@ int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
   a.status = reinterpret_cast<int*>(ws);
   a.counters = reinterpret_cast<unsigned*>(ws + kAlign);
   return cuda_status(launch_accept(a, logits_dtype, stream));
+}
+
+int mt_tree_accept_typical(int batch, int tree_size, int vocab, int max_depth,
+                           mt_dtype logits_dtype, const int32_t* tree_tokens,
+                           const void* target_logits, const int32_t* tree_parents,
+                           float temperature, float epsilon, float delta, int32_t* node_accept,
+                           int32_t* accept_len, int32_t* accept_path, int32_t* next_token,
+                           void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  if (batch < 1 || batch > (1 << 24) / kMaxTree) return MT_ERR_INVALID_ARG;
+  if (tree_size < 1 || tree_size > kMaxTree) return MT_ERR_UNSUPPORTED;
+  if (vocab < 1 || max_depth < 0 || max_depth >= kMaxTree) return MT_ERR_INVALID_ARG;
+  if (logits_dtype != MT_F32 && logits_dtype != MT_F16 && logits_dtype != MT_BF16)
+    return MT_ERR_UNSUPPORTED;
+  const float k = (float)(1.4426950408889634 / (double)temperature);
+  if (!(temperature > 0.f) || !std::isfinite(temperature) || !std::isfinite(k) || !(epsilon > 0.f) ||
+      !std::isfinite(epsilon) || !(delta > 0.f) || !std::isfinite(delta))
+    return MT_ERR_INVALID_ARG;
+  if (!tree_tokens || !target_logits || !tree_parents || !node_accept || !accept_len ||
+      !accept_path || !next_token || !workspace)
+    return MT_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(workspace) % kAlign) ||
+      ws_bytes < mt_tree_accept_workspace_size(batch, tree_size))
+    return MT_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  const AcceptWs w = accept_ws(batch, tree_size);
+  AcceptParams a{};
+  a.B = batch; a.T = tree_size; a.V = vocab; a.max_depth = max_depth;
+  a.tokens = tree_tokens; a.logits = target_logits; a.parents = tree_parents;
+  a.argmax_out = reinterpret_cast<int*>(ws + w.argmax);
+  a.accept_len = accept_len; a.accept_path = accept_path; a.next_token = next_token;
+  a.status = reinterpret_cast<int*>(ws);
+  a.counters = reinterpret_cast<unsigned*>(ws + w.counters);
+  TypicalParams t{};
+  t.k = k; t.epsilon = epsilon; t.delta = delta;
+  t.stats = reinterpret_cast<float4*>(ws + w.stats);
+  t.node_accept = node_accept;
+  return cuda_status(launch_accept_typical(a, t, logits_dtype, stream));
 }
 
 int mt_kv_commit(const mt_attn_desc* d, int max_depth, const int32_t* accept_path,

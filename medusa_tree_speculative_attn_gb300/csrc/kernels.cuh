@@ -82,6 +82,14 @@ struct AcceptParams {
   unsigned int* counters;  // [B], left at zero
 };
 
+// Typical acceptance's extra arguments (accept.cu).
+struct TypicalParams {
+  float k;                 // log2(e) / temperature
+  float epsilon, delta;    // threshold min(epsilon, delta * exp(-entropy))
+  float4* stats;           // [B*T] per row (max of y, Z, threshold, unused), workspace
+  int* node_accept;        // [B][T] each node's own test (1 at the root)
+};
+
 struct CommitParams {
   int B, T, Hkv, D, P, max_blocks, num_pages, max_depth, rel_width, elem_bytes;
   const int* accept_path;
@@ -122,6 +130,7 @@ cudaError_t launch_cand(const CandParams& a, int dtype, cudaStream_t stream);
 cudaError_t launch_accept(const AcceptParams& a, int dtype, cudaStream_t stream);
 // Acceptance and, per sequence as soon as its path is known, the KV commit.
 cudaError_t launch_accept_commit(const AcceptParams& a, const CommitParams& c, int dtype, cudaStream_t stream);
+cudaError_t launch_accept_typical(const AcceptParams& a, const TypicalParams& t, int dtype, cudaStream_t stream);
 cudaError_t launch_commit(const CommitParams& a, cudaStream_t stream);
 
 }  // namespace mt
