@@ -117,6 +117,29 @@ def _need(t: torch.Tensor, name: str, dtype=None, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
 
 
+def _shape(t: torch.Tensor, name: str, shape):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _min_bytes(t: torch.Tensor, name: str, n: int):
+    if t.numel() * t.element_size() < n:
+        raise ValueError(f"{name} must hold at least {n} bytes")
+
+
+def _on_device(**tensors):
+    """Every tensor on the first one's CUDA device: the kernels dereference the
+    pointers as device memory, so a host tensor must never reach them."""
+    dev = None
+    for name, t in tensors.items():
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be on a CUDA device, got {t.device}")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other tensors on {dev}")
+
+
 class Rope:
     """Library-owned fp32 cos/sin table on the current device."""
 
@@ -197,7 +220,21 @@ def tree_attn_paged(q, k_cache, v_cache, block_tables, seq_lens, tree_parents, t
         _need(t, name, torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     _need(workspace, "workspace")
+    B, T, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _shape(t, name, (B, T, Hkv, D))
+    _shape(out, "out", q.shape)
+    _shape(v_cache, "v_cache", k_cache.shape)
+    _shape(seq_lens, "seq_lens", (B,))
+    if block_tables.shape[0] != B:
+        raise ValueError("block_tables must have one row per sequence")
+    for name, t in (("tree_parents", tree_parents), ("tree_depths", tree_depths)):
+        _shape(t, name, (B, T))
     desc = make_desc(q, k_cache, block_tables, num_splits, kernel, sm_scale, k_scale, v_scale)
+    _on_device(q=q, k_new=k_new, v_new=v_new, out=out, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, seq_lens=seq_lens, tree_parents=tree_parents,
+               tree_depths=tree_depths, workspace=workspace)
     st = _load().mt_tree_attn_paged(ctypes.byref(desc), _ptr(q), _ptr(k_new), _ptr(v_new),
                                     _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                     _ptr(seq_lens), _ptr(tree_parents), _ptr(tree_depths),
@@ -218,12 +255,18 @@ def tree_accept_greedy(tree_tokens, target_logits, tree_parents, accept_len, acc
         _need(t, name, torch.int32, 1)
     _need(accept_path, "accept_path", torch.int32, 2)
     _need(argmax_out, "argmax_out", torch.int32, 2)
+    _need(workspace, "workspace")
     B, T = tree_tokens.shape
     V = target_logits.shape[2]
     if max_depth is None:
         max_depth = accept_path.shape[1] - 1
     if accept_path.shape[1] != max_depth + 1:
         raise ValueError("accept_path must have max_depth + 1 columns")
+    _accept_shapes(B, T, V, target_logits, tree_parents, accept_len, accept_path, next_token,
+                   argmax_out=argmax_out)
+    _on_device(tree_tokens=tree_tokens, target_logits=target_logits, tree_parents=tree_parents,
+               argmax_out=argmax_out, accept_len=accept_len, accept_path=accept_path,
+               next_token=next_token, workspace=workspace)
     st = _load().mt_tree_accept_greedy(B, T, V, int(max_depth), _DTYPES[target_logits.dtype],
                                        _ptr(tree_tokens), _ptr(target_logits), _ptr(tree_parents),
                                        _ptr(argmax_out), _ptr(accept_len), _ptr(accept_path),
@@ -231,6 +274,17 @@ def tree_accept_greedy(tree_tokens, target_logits, tree_parents, accept_len, acc
                                        workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st, "mt_tree_accept_greedy")
     return accept_len, accept_path
+
+
+def _accept_shapes(B, T, V, target_logits, tree_parents, accept_len, accept_path, next_token, **per_node):
+    _shape(target_logits, "target_logits", (B, T, V))
+    _shape(tree_parents, "tree_parents", (B, T))
+    _shape(accept_len, "accept_len", (B,))
+    _shape(next_token, "next_token", (B,))
+    if accept_path.shape[0] != B:
+        raise ValueError("accept_path must have one row per sequence")
+    for name, t in per_node.items():
+        _shape(t, name, (B, T))
 
 
 def tree_accept_typical(tree_tokens, target_logits, tree_parents, accept_len, accept_path, *,
@@ -246,12 +300,18 @@ def tree_accept_typical(tree_tokens, target_logits, tree_parents, accept_len, ac
         _need(t, name, torch.int32, 1)
     _need(accept_path, "accept_path", torch.int32, 2)
     _need(node_accept, "node_accept", torch.int32, 2)
+    _need(workspace, "workspace")
     B, T = tree_tokens.shape
     V = target_logits.shape[2]
     if max_depth is None:
         max_depth = accept_path.shape[1] - 1
     if accept_path.shape[1] != max_depth + 1:
         raise ValueError("accept_path must have max_depth + 1 columns")
+    _accept_shapes(B, T, V, target_logits, tree_parents, accept_len, accept_path, next_token,
+                   node_accept=node_accept)
+    _on_device(tree_tokens=tree_tokens, target_logits=target_logits, tree_parents=tree_parents,
+               node_accept=node_accept, accept_len=accept_len, accept_path=accept_path,
+               next_token=next_token, workspace=workspace)
     st = _load().mt_tree_accept_typical(B, T, V, int(max_depth), _DTYPES[target_logits.dtype],
                                         _ptr(tree_tokens), _ptr(target_logits), _ptr(tree_parents),
                                         float(temperature), float(epsilon), float(delta),
@@ -276,11 +336,21 @@ def kv_commit(accept_path, accept_len, k_cache, v_cache, block_tables, seq_lens,
     _need(released_pages, "released_pages", torch.int32, 2)
     _need(k_cache, "k_cache", None, 4)
     _need(v_cache, "v_cache", k_cache.dtype, 4)
+    _need(status_ws, "status_ws")
     P = k_cache.shape[2]
     B = block_tables.shape[0]
     if released_pages.shape != (B, released_width(tree_size, P)):
         raise ValueError("released_pages must be [B, (T + 2P - 2) // P]")
+    _shape(v_cache, "v_cache", k_cache.shape)
+    _shape(accept_len, "accept_len", (B,))
+    _shape(seq_lens, "seq_lens", (B,))
+    if accept_path.shape[0] != B:
+        raise ValueError("accept_path must have one row per sequence")
+    _min_bytes(status_ws, "status_ws", 256)
     desc = _commit_desc(B, int(tree_size), k_cache, block_tables.shape[1])
+    _on_device(accept_path=accept_path, accept_len=accept_len, k_cache=k_cache, v_cache=v_cache,
+               block_tables=block_tables, seq_lens=seq_lens, released_pages=released_pages,
+               status_ws=status_ws)
     st = _load().mt_kv_commit(ctypes.byref(desc), accept_path.shape[1] - 1, _ptr(accept_path),
                               _ptr(accept_len), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                               _ptr(seq_lens), _ptr(released_pages), _ptr(status_ws), _stream(stream))
@@ -311,7 +381,17 @@ def tree_accept_commit(tree_tokens, target_logits, tree_parents, accept_len, acc
     P = k_cache.shape[2]
     if released_pages.shape != (B, released_width(T, P)):
         raise ValueError("released_pages must be [B, (T + 2P - 2) // P]")
+    _accept_shapes(B, T, V, target_logits, tree_parents, accept_len, accept_path, next_token,
+                   argmax_out=argmax_out)
+    _shape(v_cache, "v_cache", k_cache.shape)
+    _shape(seq_lens, "seq_lens", (B,))
+    if block_tables.shape[0] != B:
+        raise ValueError("block_tables must have one row per sequence")
     desc = _commit_desc(B, int(T), k_cache, block_tables.shape[1])
+    _on_device(tree_tokens=tree_tokens, target_logits=target_logits, tree_parents=tree_parents,
+               argmax_out=argmax_out, accept_len=accept_len, accept_path=accept_path,
+               next_token=next_token, k_cache=k_cache, v_cache=v_cache, block_tables=block_tables,
+               seq_lens=seq_lens, released_pages=released_pages, workspace=workspace)
     st = _load().mt_tree_accept_commit(ctypes.byref(desc), V, int(max_depth),
                                        _DTYPES[target_logits.dtype], _ptr(tree_tokens),
                                        _ptr(target_logits), _ptr(tree_parents), _ptr(argmax_out),
@@ -339,6 +419,10 @@ def tree_candidates(root_logits, head_logits, tree_parents, tree_tokens, *, stat
     T = tree_parents.shape[1]
     if tree_parents.shape != (B, T) or tree_tokens.shape != (B, T):
         raise ValueError("tree_parents and tree_tokens must be [B, T]")
+    _need(status_ws, "status_ws")
+    _min_bytes(status_ws, "status_ws", 256)
+    _on_device(root_logits=root_logits, head_logits=head_logits, tree_parents=tree_parents,
+               tree_tokens=tree_tokens, status_ws=status_ws)
     st = _load().mt_tree_candidates(B, T, heads, V, _DTYPES[root_logits.dtype], _ptr(root_logits),
                                     _ptr(head_logits), _ptr(tree_parents), _ptr(tree_tokens),
                                     _ptr(status_ws), _stream(stream))
@@ -348,6 +432,9 @@ def tree_candidates(root_logits, head_logits, tree_parents, tree_tokens, *, stat
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:
     """Synchronises the stream, returns and clears the device status word."""
+    _need(workspace, "workspace")
+    _min_bytes(workspace, "workspace", 4)
+    _on_device(workspace=workspace)
     v = ctypes.c_int(0)
     _check(_load().mt_read_status(_ptr(workspace), _stream(stream), ctypes.byref(v)), "mt_read_status")
     return v.value
