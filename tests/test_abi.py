@@ -4,6 +4,8 @@ before touching the device."""
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -196,3 +198,34 @@ def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mt, "_lib", None)
     with pytest.raises(RuntimeError):
         mt.library()
+
+
+C_PROGRAM = r"""
+#include "medusa_tree.h"
+#include <stdio.h>
+int main(void) {
+  mt_attn_desc d = {0};
+  d.batch = 2; d.tree_size = 8; d.num_q_heads = 8; d.num_kv_heads = 2; d.head_dim = 96;
+  d.page_size = 16; d.max_blocks_per_seq = 4; d.num_pages = 8; d.dtype = MT_BF16;
+  printf("%d %d %zu\n", mt_version(), (int)mt_tree_attn_workspace_size(&d),
+         mt_tree_accept_workspace_size(0, 8));
+  return 0;
+}
+"""
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    from medusa_tree_speculative_attn_gb300 import LIB_PATH
+    src = tmp_path / "use_abi.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "use_abi"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    libdir = os.path.dirname(LIB_PATH)
+    subprocess.check_call([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           "-I", cuda_inc, str(src), "-o", str(exe), "-L", libdir, "-lmedusa_tree",
+                           "-Wl,-rpath," + libdir])
+    out = subprocess.check_output([str(exe)]).decode().split()
+    assert out == ["10000", "0", "0"]   # version; head_dim 96 refused (size 0); empty batch
