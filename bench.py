@@ -2,7 +2,8 @@
 
 One step = tree_attn_paged + tree_accept_commit (greedy acceptance and the KV
 commit in one launch; ``--accept separate`` runs tree_accept_greedy then
-kv_commit instead) over one batch of
+kv_commit instead, ``--accept typical`` tree_accept_typical then kv_commit)
+over one batch of
 the serving workload (batch 16, 32 q / 8 kv heads, D 128, bf16, prefixes
 uniform in [512, 8192], 64-node trees, bf16 logits over a 32000 vocab), inputs
 resident in HBM.  Between steps (outside the timed events) the block tables and
@@ -45,8 +46,12 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
-    ap.add_argument("--accept", default="fused", choices=["fused", "separate"],
-                    help="acceptance and commit in one launch, or as the two calls")
+    ap.add_argument("--accept", default="fused", choices=["fused", "separate", "typical"],
+                    help="greedy acceptance and commit in one launch, as the two calls, or "
+                         "typical acceptance then the commit")
+    ap.add_argument("--temperature", type=float, default=1.0, help="typical acceptance")
+    ap.add_argument("--epsilon", type=float, default=0.09, help="typical acceptance")
+    ap.add_argument("--delta", type=float, default=0.3, help="typical acceptance")
     return ap.parse_args()
 
 
@@ -261,7 +266,9 @@ def run_ours(args, rank, world, local_rank):
     alen = torch.empty(B, dtype=torch.int32, device=dev)
     path = torch.empty((B, md + 1), dtype=torch.int32, device=dev)
     nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    node_ok = torch.empty((B, T), dtype=torch.int32, device=dev)
     rel = torch.empty((B, mt.released_width(T, w["page_size"])), dtype=torch.int32, device=dev)
+    typical = dict(temperature=args.temperature, epsilon=args.epsilon, delta=args.delta)
     bt0, sl0 = w["block_tables"].clone(), w["seq_lens"].clone()
     has_accept = "logits" in w
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -280,8 +287,12 @@ def run_ours(args, rank, world, local_rank):
                                   w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
                                   argmax_out=am, next_token=nxt, workspace=aws)
         elif has_accept:
-            mt.tree_accept_greedy(s["tree_tokens"], s["logits"], s["tree_parents"], alen, path,
-                                  argmax_out=am, next_token=nxt, workspace=aws)
+            if args.accept == "typical":
+                mt.tree_accept_typical(s["tree_tokens"], s["logits"], s["tree_parents"], alen, path,
+                                       node_accept=node_ok, next_token=nxt, workspace=aws, **typical)
+            else:
+                mt.tree_accept_greedy(s["tree_tokens"], s["logits"], s["tree_parents"], alen, path,
+                                      argmax_out=am, next_token=nxt, workspace=aws)
             mt.kv_commit(path, alen, w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
                          tree_size=T, status_ws=ws)
 
@@ -298,6 +309,7 @@ def run_ours(args, rank, world, local_rank):
     # duration (library profiling hook), kernels launched one by one
     mk = lambda: torch.cuda.Event(enable_timing=True)
     evb = [(mk(), mk(), mk(), mk(), mk(), mk()) for _ in range(K)]
+    evt = [(mk(), mk()) for _ in range(K)] if has_accept and args.accept == "typical" else []
     mt.profile_enable(K)
     for k in range(K):
         restore()
@@ -322,6 +334,12 @@ def run_ours(args, rank, world, local_rank):
                                   w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
                                   argmax_out=am, next_token=nxt, workspace=aws)
             e5.record(stream)
+            if evt:
+                flush.fill_(k & 0xFF)
+                evt[k][0].record(stream)
+                mt.tree_accept_typical(w["tree_tokens"], w["logits"], w["tree_parents"], alen, path,
+                                       node_accept=node_ok, next_token=nxt, workspace=aws, **typical)
+                evt[k][1].record(stream)
         else:
             for e in (e2, e3, e4, e5):
                 e.record(stream)
@@ -334,8 +352,12 @@ def run_ours(args, rank, world, local_rank):
                  "tree_accept_greedy_ms": avg(1, 2), "kv_commit_ms": avg(2, 3),
                  "tree_accept_commit_ms": avg(4, 5),
                  "note": "each call timed alone, L2 flushed before the attention and before the "
-                         "fused call; the step uses " + ("tree_accept_commit" if args.accept == "fused"
-                                                          else "tree_accept_greedy + kv_commit")}
+                         "fused call" + (" and the typical call" if evt else "") + "; the step uses " + {
+                             "fused": "tree_accept_commit", "separate": "tree_accept_greedy + kv_commit",
+                             "typical": "tree_accept_typical + kv_commit"}[args.accept]}
+    if evt:
+        breakdown["tree_accept_typical_ms"] = float(np.mean([a.elapsed_time(b) for a, b in evt]))
+        breakdown["typical"] = typical
 
     # (2) the timed steps: the whole step replayed as one CUDA graph (or
     # launched kernel by kernel with --no-graph)
@@ -396,7 +418,8 @@ def run_ours(args, rank, world, local_rank):
             keys_in += ["tree_tokens", "logits"]
         host = {k: w[k].cpu().pin_memory() for k in keys_in}
         dsrc = {k: torch.empty_like(w[k]) for k in keys_in}
-        outs = [out, am, alen, path, nxt, rel] if has_accept else [out]
+        per_node = node_ok if args.accept == "typical" else am
+        outs = [out, per_node, alen, path, nxt, rel] if has_accept else [out]
         houts = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
         h2d = sum(host[k].numel() * host[k].element_size() for k in keys_in)
         d2h = sum(o.numel() * o.element_size() for o in outs)
