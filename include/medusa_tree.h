@@ -259,7 +259,8 @@ int mt_tree_accept_typical(int batch, int tree_size, int vocab, int max_depth,
  *   accept_path int32 [B][max_depth+1], accept_len int32 [B] (as produced by
  *   mt_tree_accept_greedy); k_cache, v_cache, block_tables, seq_lens are
  *   updated in place.  desc supplies B, T, Hkv, D, P, max_blocks_per_seq,
- *   num_pages and dtype.  status_ws: at least 256 bytes of device memory whose
+ *   num_pages and the element size: dtype's, or 1 byte when cache_dtype is
+ *   MT_E4M3 (the codes move unchanged).  status_ws: at least 256 bytes of device memory whose
  *   first int32 is the device status word (the attention workspace serves). */
 int mt_kv_commit(const mt_attn_desc* desc, int max_depth, const int32_t* accept_path,
                  const int32_t* accept_len, void* k_cache, void* v_cache,
@@ -272,8 +273,8 @@ int mt_kv_commit(const mt_attn_desc* desc, int max_depth, const int32_t* accept_
  * sequence is committed as soon as its path is known, by the CTA that
  * completed its argmax rows, so the step has no launch or round trip between
  * acceptance and commit.  desc supplies B (batch), T (tree_size), Hkv, D, P,
- * max_blocks_per_seq, num_pages and the cache dtype; the logits have their own
- * dtype.  workspace: mt_tree_accept_workspace_size(B, T) bytes, zero-filled
+ * max_blocks_per_seq, num_pages and the cache's element size (as for
+ * mt_kv_commit); the logits have their own dtype.  workspace: mt_tree_accept_workspace_size(B, T) bytes, zero-filled
  * before first use; its first int32 is the device status word, which records
  * the acceptance errors (MT_ERR_TREE) and the commit errors (MT_ERR_PAGES) of
  * both calls.  Host errors: those of the two calls.  A sequence whose tree is
