@@ -315,7 +315,7 @@ int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
   a.argmax_out = argmax_out; a.accept_len = accept_len; a.accept_path = accept_path;
   a.next_token = next_token;
   a.status = reinterpret_cast<int*>(ws);
-  a.counters = reinterpret_cast<unsigned*>(ws + kAlign);
+  a.counters = reinterpret_cast<unsigned*>(ws + accept_ws(batch, tree_size).counters);
   return cuda_status(launch_accept(a, logits_dtype, stream));
 }
 
@@ -408,7 +408,7 @@ int mt_tree_accept_commit(const mt_attn_desc* d, int vocab, int max_depth, mt_dt
   a.argmax_out = argmax_out; a.accept_len = accept_len; a.accept_path = accept_path;
   a.next_token = next_token;
   a.status = reinterpret_cast<int*>(ws);
-  a.counters = reinterpret_cast<unsigned*>(ws + kAlign);
+  a.counters = reinterpret_cast<unsigned*>(ws + accept_ws(batch, tree_size).counters);
   CommitParams c{};
   c.B = batch; c.T = tree_size; c.Hkv = d->num_kv_heads; c.D = d->head_dim;
   c.P = d->page_size; c.max_blocks = d->max_blocks_per_seq; c.num_pages = d->num_pages;
