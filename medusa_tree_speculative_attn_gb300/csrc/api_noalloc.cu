@@ -7,9 +7,11 @@
 // code cannot use the array's name as a device address, so the first call on
 // each device (with that device current) asks the runtime for the address
 // with cudaGetSymbolAddress and keeps it; that first call should therefore
-// come before any stream capture.  All calls on a device share the one array:
-// calls whose kernels overlap on the GPU race with each other, so callers
-// serialise them (one stream, or events).
+// come before any stream capture.  The address is kept for the life of the
+// process: a cudaDeviceReset after the first call on a device may move the
+// array, so this entry point is not supported across a device reset.  All
+// calls on a device share the one array: calls whose kernels overlap on the
+// GPU race with each other, so callers serialise them (one stream, or events).
 #include <mutex>
 
 #include "../../include/medusa_tree.h"
@@ -47,7 +49,9 @@ extern "C" int mt_tree_attn_paged_noalloc(const mt_attn_desc* desc, const void* 
                                           const mt_rope* rope, void* out, int32_t* device_status,
                                           cudaStream_t stream) {
   const size_t need = mt_tree_attn_workspace_size(desc);
-  if (need == 0) return desc ? MT_ERR_UNSUPPORTED : MT_ERR_INVALID_ARG;
+  if (need == 0)  // an invalid descriptor: the workspace call reports why, launching nothing
+    return mt_tree_attn_paged(desc, q, k_new, v_new, k_cache, v_cache, block_tables, seq_lens, tree_parents,
+                              tree_depths, rope, out, nullptr, 0, stream);
   if (need > kNoallocScratchBytes) return MT_ERR_UNSUPPORTED;  // workspace exceeds the fixed array
   void* scratch = nullptr;
   int st = scratch_address(&scratch);

@@ -21,7 +21,18 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import act_to_f64
+
+def act_to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Widen act-dtype values to float64 with NumPy's own conversions, not the
+    C oracle's decoder, so that the brute force does not inherit a slip in it:
+    fp16 through NumPy's binary16 type; bf16 as the upper half of a float32
+    (the bfloat16 layout), read by NumPy as float32."""
+    if dtype == "f32":
+        return np.asarray(x, np.float32).astype(np.float64)
+    if dtype == "f16":
+        return np.asarray(x, np.float16).astype(np.float64)
+    bits = np.asarray(x, np.uint16).astype(np.uint32) << 16
+    return bits.view(np.float32).astype(np.float64)
 
 
 def ancestor_matrix(parents) -> np.ndarray:

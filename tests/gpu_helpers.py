@@ -108,20 +108,3 @@ class Step:
 def _host(w, key):
     v = w.get(key + "_host", w[key])
     return v.cpu().numpy() if isinstance(v, torch.Tensor) else v
-
-
-def sample_triples(w: dict, n: int, seed: int = 0) -> np.ndarray:
-    """(b, h, i) triples: the extremes plus a seeded random sample."""
-    rng = np.random.default_rng(seed)
-    B, T, Hq = w["B"], w["T"], w["Hq"]
-    seq = _host(w, "seq_lens")
-    depths = _host(w, "tree_depths")
-    picks = set()
-    bmax, bmin = int(np.argmax(seq)), int(np.argmin(seq))
-    for b in (0, B - 1, bmax, bmin):
-        for h in (0, Hq - 1):
-            for i in (0, T - 1, int(np.argmax(depths[b]))):
-                picks.add((b, h, i))
-    while len(picks) < n:
-        picks.add((int(rng.integers(B)), int(rng.integers(Hq)), int(rng.integers(T))))
-    return np.array(sorted(picks), dtype=np.int32)

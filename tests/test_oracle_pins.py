@@ -69,6 +69,43 @@ def test_bf16_rounding_is_nearest_even():
     assert np.array_equal(got, want)
 
 
+def _same_f64(got, want):
+    # equal values, NaN where NaN, and the sign of every zero
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_f16_widening_matches_numpy_on_every_code():
+    # every binary16 bit pattern: zeros, subnormals, normals, infinities, NaNs
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = codes.view(np.float16)
+    got = oracle.act_to_f64(x, "f16")
+    _same_f64(got, x.astype(np.float64))
+    # a few values the format fixes, read off its definition
+    assert got[0x0001] == 2.0**-24 and got[0x03FF] == 1023 * 2.0**-24
+    assert got[0x0400] == 2.0**-14 and got[0x3C00] == 1.0 and got[0x7BFF] == 65504.0
+    assert got[0x7C00] == np.inf and got[0xFC00] == -np.inf and np.isnan(got[0x7E00])
+    assert got[0x8000] == 0.0 and np.signbit(got[0x8000])
+
+
+def test_bf16_widening_matches_torch_on_every_code():
+    torch = pytest.importorskip("torch")
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.act_to_f64(codes, "bf16")
+    want = torch.from_numpy(codes.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    _same_f64(got, want)
+    assert got[0x0001] == 2.0**-133 and got[0x0080] == 2.0**-126 and got[0x3F80] == 1.0
+    assert got[0x7F7F] == 255 * 2.0**120 and got[0x7F80] == np.inf and np.isnan(got[0x7FC0])
+    assert got[0xC000] == -2.0
+
+
+def test_f32_widening_is_exact():
+    x = _edge_floats()
+    _same_f64(oracle.act_to_f64(x, "f32"), x.astype(np.float64))
+
+
 def test_bf16_rounding_matches_torch():
     torch = pytest.importorskip("torch")
     x = _edge_floats()
