@@ -334,6 +334,21 @@ const char* mt_status_string(int status);
 int mt_profile_enable(int max_records);
 int mt_profile_read(float* ms, int max_records, int* n_out);
 
+/* ---- Timeout test hook --------------------------------------------------------
+ * Every pipeline wait of the tensor-core attention kernel (a TMA load landing,
+ * an MMA completing, a softmax handing over P) gives up after a bounded time:
+ * the kernel then records MT_ERR_TIMEOUT in the status word, lets its other
+ * warps stop, waits for its own copies and MMAs in flight, frees its tensor
+ * memory and returns, leaving the context usable.  mt_debug_set_wait sets that
+ * bound for later mt_tree_attn_paged calls (limit_ns 0 restores the default of
+ * 2 s); stall = 1 makes the kernel first wait on a barrier that nothing
+ * completes, so that the bound always expires (for tests of the timeout path;
+ * stall = 0 is normal operation).  Process-wide, not thread-safe.  Returns
+ * MT_ERR_INVALID_ARG for a stall other than 0 or 1.  Not on the pages: the
+ * wait bound is how this library reports a stalled pipeline instead of
+ * hanging the GPU. */
+int mt_debug_set_wait(unsigned long long limit_ns, int stall);
+
 /* Version of this ABI: major * 10000 + minor * 100 + patch. */
 int mt_version(void);
 

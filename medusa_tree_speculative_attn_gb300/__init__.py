@@ -78,6 +78,7 @@ def _load():
         lib.mt_read_status.argtypes = [P, P, ctypes.POINTER(I)]
         lib.mt_profile_enable.argtypes = [I]
         lib.mt_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), I, ctypes.POINTER(I)]
+        lib.mt_debug_set_wait.argtypes = [ctypes.c_ulonglong, I]
         _lib = lib
     return _lib
 
@@ -451,6 +452,13 @@ def profile_read(max_records: int = 65536):
     n = ctypes.c_int(0)
     _check(_load().mt_profile_read(buf, max_records, ctypes.byref(n)), "mt_profile_read")
     return [buf[i] for i in range(n.value)]
+
+
+def debug_set_wait(limit_ns: int = 0, stall: bool = False):
+    """Bound of the tensor-core kernel's pipeline waits for later attention
+    calls (0: the default, 2 s); stall=True makes its first wait one that only
+    a timeout ends (tests of the timeout path)."""
+    _check(_load().mt_debug_set_wait(int(limit_ns), 1 if stall else 0), "mt_debug_set_wait")
 
 
 def version() -> int:

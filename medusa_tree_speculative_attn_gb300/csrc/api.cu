@@ -8,6 +8,11 @@
 #include "../../include/medusa_tree.h"
 #include "kernels.cuh"
 
+// Bound of the tensor-core kernel's pipeline waits, and the timeout test hook
+// (mt_debug_set_wait); read by every attention call.
+static unsigned long long g_wait_limit_ns = 0;  // 0: the default (2 s)
+static int g_wait_stall = 0;
+
 // Optional timing of the main attention kernel (profiling hook, one host thread).
 static cudaEvent_t* g_prof_ev = nullptr;  // [cap][2]
 static int g_prof_cap = 0;
@@ -249,6 +254,8 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   ap.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   ap.sched = sched;
   ap.piece_table = pp.piece_table;
+  ap.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : 2000000000ull;
+  ap.test_stall = g_wait_stall;
   const bool prof = g_prof_n < g_prof_cap;
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);
   if (kernel == MT_KERNEL_SIMT) {
@@ -473,6 +480,13 @@ int mt_profile_read(float* ms, int max_records, int* n_out) {
   }
   *n_out = n;
   g_prof_n = 0;
+  return MT_OK;
+}
+
+int mt_debug_set_wait(unsigned long long limit_ns, int stall) {
+  if (stall != 0 && stall != 1) return MT_ERR_INVALID_ARG;
+  g_wait_limit_ns = limit_ns;
+  g_wait_stall = stall;
   return MT_OK;
 }
 

@@ -34,9 +34,11 @@
 // Shared memory holds Q staging (up to 64 KB), P (16 KB per M tile) and a
 // ring of 32 KB K/V stages; TMEM holds O (2 x 128 columns), S (2 x 64) and Q
 // (2 x 64 packed 16-bit pairs).
-// Every mbarrier wait is bounded (2 s); on a timeout the kernel records
-// MT_ERR_TIMEOUT, lets the other roles bail out, waits for its own TMA loads
-// and MMAs, frees TMEM and returns.
+// Tensor-core instructions are issued by the elected lane of a converged warp
+// (tc::elect_one), which issues about twice as fast as a lane-0 branch.
+// Every mbarrier wait is bounded (2 s unless the caller set another limit);
+// on a timeout the kernel records MT_ERR_TIMEOUT, lets the other roles bail
+// out, waits for its own TMA loads and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <type_traits>
@@ -111,7 +113,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
   const uint64_t t0 = tc::global_timer_ns();
   while (!tc::mbar_try_wait(bar, parity)) {
-    if (tc::global_timer_ns() - t0 > tc::kWaitLimitNs) {
+    if (tc::global_timer_ns() - t0 > tc::kDrainLimitNs) {
       set_status(status, kStTimeout);
       return;
     }
@@ -161,7 +163,8 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   uint64_t* q_empty = q_full + 1;       // every Q K^T of the previous piece done
   uint64_t* o_free = q_empty + 1;       // O of the previous piece read out
   uint64_t* fin = o_free + 1;           // [2] every MMA of each issuer done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 2);
+  uint64_t* never = fin + 2;            // nothing arrives here (timeout test hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_npieces = const_cast<int*>(abort_flag + 1);
   PieceRec* s_pieces = reinterpret_cast<PieceRec*>(reinterpret_cast<uint8_t*>(bars) + 1024);
@@ -181,6 +184,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     }
     tc::mbar_init(&fin[0], 1);
     tc::mbar_init(&fin[1], 1);
+    tc::mbar_init(never, 1);
     tc::mbar_init(q_full, 1);
     tc::mbar_init(q_empty, 1);
     tc::mbar_init(o_free, C::kSoftmaxWarps);
@@ -212,6 +216,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sQ_u = tc::smem_u32(sQ), sKV_u = tc::smem_u32(sKV), sP_u = tc::smem_u32(sP);
+  const uint64_t limit = a.wait_limit_ns;
 
   if (warp >= C::kProducer0) {
     // ----------------------------------------------------------- producers
@@ -231,7 +236,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     uint32_t it = 0, npieces = 0, nq = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      bool r = tc::mbar_wait(bar, parity, abort_flag, a.status);
+      bool r = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
       ok = __all_sync(0xffffffffu, r) && ok;
     };
     auto issue_q = [&]() {
@@ -320,25 +325,25 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     uint32_t it = 0, npieces = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      bool r = tc::mbar_wait(bar, parity, abort_flag, a.status);
+      bool r = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
       ok = __all_sync(0xffffffffu, r) && ok;
     };
+    if (a.test_stall) wait_all(never, 0);  // test hook: a wait that can only time out
     while (ok && pi.next(pc, pL)) {
       // the piece's queries: shared memory -> TMEM (after every Q K^T of the
       // previous piece, in issue order), then the staging buffer is free
       wait_all(q_full, npieces & 1);
       if (!ok) break;
       tc::tc_fence_after();
-      if (lane == 0) {
-        for (int m = 0; m < MT; ++m)
+      for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t h = kk / 4, k4 = kk % 4;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t h = kk / 4, k4 = kk % 4;
+          if (tc::elect_one())
             tc::tmem_cp_128x256b(tmem + C::q_col(m) + kk * 8,
                                  tc::smem_desc(sQ_u + (m * C::NH + h) * (128 * 128) + k4 * 32, 16, 1024));
-          }
-        tc::mma_commit(q_empty);
-      }
+        }
+      if (tc::elect_one()) tc::mma_commit(q_empty);
       __syncwarp();
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
         const uint32_t stage = it % S;
@@ -355,26 +360,26 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
             if (!ok) break;
           }
           tc::tc_fence_after();
-          if (lane == 0) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t h = kk / 4, k4 = kk % 4;
-              const uint64_t bd = kd0 + (uint64_t)((h * C::kHalfTile + k4 * 32) >> 4);
-              if (kk == 0) tc::mma_f16_ts<false>(tmem + C::s_col(m), tmem + C::q_col(m) + kk * 8, bd, kIdescQK);
-              else tc::mma_f16_ts<true>(tmem + C::s_col(m), tmem + C::q_col(m) + kk * 8, bd, kIdescQK);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t h = kk / 4, k4 = kk % 4;
+            const uint64_t bd = kd0 + (uint64_t)((h * C::kHalfTile + k4 * 32) >> 4);
+            if (kk == 0) {
+              if (tc::elect_one()) tc::mma_f16_ts<false>(tmem + C::s_col(m), tmem + C::q_col(m), bd, kIdescQK);
+            } else {
+              if (tc::elect_one()) tc::mma_f16_ts<true>(tmem + C::s_col(m), tmem + C::q_col(m) + kk * 8, bd, kIdescQK);
             }
-            tc::mma_commit(&s_full[m]);
           }
+          if (tc::elect_one()) tc::mma_commit(&s_full[m]);
           __syncwarp();
         }
         if (!ok) break;
       }
       ++npieces;
     }
-    if (lane == 0) {
-      tc::mma_commit(&fin[0]);
-      drain_wait(&fin[0], 0, a.status);
-    }
+    if (tc::elect_one()) tc::mma_commit(&fin[0]);
+    __syncwarp();
+    if (lane == 0) drain_wait(&fin[0], 0, a.status);
     __syncwarp();
   } else if (warp == C::kPvWarp) {
     // ---------------------------------------------------------- PV issuer
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     uint32_t it = 0, npieces = 0;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      bool r = tc::mbar_wait(bar, parity, abort_flag, a.status);
+      bool r = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
       ok = __all_sync(0xffffffffu, r) && ok;
     };
     while (ok && pi.next(pc, pL)) {
@@ -416,31 +421,29 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
           wait_all(&p_full[m], it & 1);
           if (!ok) break;
           tc::tc_fence_after();
-          if (lane == 0) {
-            const uint32_t d_t = tmem + C::o_col(m);
-            const uint32_t p_u = sP_u + m * C::kPTile;
-            const uint64_t pd0 = tc::smem_desc(p_u, 16, 1024), vd0 = tc::smem_desc(v_u, C::kHalfTile, 1024);
-            if (first)
-              tc::mma_f16_ss<false>(d_t, pd0, vd0, kIdescPV);
-            else
-              tc::mma_f16_ss<true>(d_t, pd0, vd0, kIdescPV);
-#pragma unroll
-            for (int kk = 1; kk < kTileKeys / 16; ++kk)  // next 16 keys: P +32 B, V +2048 B
-              tc::mma_f16_ss<true>(d_t, pd0 + (uint64_t)(kk * 2), vd0 + (uint64_t)(kk * 128), kIdescPV);
-            tc::mma_commit(&pv_done[m]);
+          const uint32_t d_t = tmem + C::o_col(m);
+          const uint32_t p_u = sP_u + m * C::kPTile;
+          const uint64_t pd0 = tc::smem_desc(p_u, 16, 1024), vd0 = tc::smem_desc(v_u, C::kHalfTile, 1024);
+          if (first) {
+            if (tc::elect_one()) tc::mma_f16_ss<false>(d_t, pd0, vd0, kIdescPV);
+          } else {
+            if (tc::elect_one()) tc::mma_f16_ss<true>(d_t, pd0, vd0, kIdescPV);
           }
+#pragma unroll
+          for (int kk = 1; kk < kTileKeys / 16; ++kk)  // next 16 keys: P +32 B, V +2048 B
+            if (tc::elect_one()) tc::mma_f16_ss<true>(d_t, pd0 + (uint64_t)(kk * 2), vd0 + (uint64_t)(kk * 128), kIdescPV);
+          if (tc::elect_one()) tc::mma_commit(&pv_done[m]);
           __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) tc::mma_commit(&empty[stage]);
+        if (tc::elect_one()) tc::mma_commit(&empty[stage]);
         __syncwarp();
       }
       ++npieces;
     }
-    if (lane == 0) {
-      tc::mma_commit(&fin[1]);
-      drain_wait(&fin[1], 0, a.status);
-    }
+    if (tc::elect_one()) tc::mma_commit(&fin[1]);
+    __syncwarp();
+    if (lane == 0) drain_wait(&fin[1], 0, a.status);
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
@@ -453,7 +456,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     constexpr int C4 = D / 4;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      bool rr = tc::mbar_wait(bar, parity, abort_flag, a.status);
+      bool rr = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
       ok = __all_sync(0xffffffffu, rr) && ok;
     };
     PieceSrc pi;

@@ -220,6 +220,8 @@ struct AttnParams {
   float2* part_ml;                // [slots][part_rows] (max in log2 units, sum)
   Sched sched;
   const int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs] (tensor-core kernel)
+  unsigned long long wait_limit_ns;  // bound of every pipeline wait (tensor-core kernel)
+  int test_stall;                    // tensor-core kernel: first wait on a barrier nothing completes
 };
 
 // A CTA's pieces, listed ahead of time by the prep kernel (up to

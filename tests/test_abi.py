@@ -33,7 +33,8 @@ def test_header_declares_the_three_calls():
     for n in ("mt_tree_attn_paged", "mt_tree_accept_greedy", "mt_kv_commit", "mt_tree_candidates",
               "mt_tree_accept_commit",
               "mt_tree_attn_workspace_size", "mt_tree_accept_workspace_size", "mt_rope_create",
-              "mt_rope_destroy", "mt_read_status", "mt_status_string", "mt_version"):
+              "mt_rope_destroy", "mt_read_status", "mt_status_string", "mt_version",
+              "mt_debug_set_wait"):
         assert n in names
 
 
@@ -229,3 +230,8 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
                            "-Wl,-rpath," + libdir])
     out = subprocess.check_output([str(exe)]).decode().split()
     assert out == ["10000", "0", "0"]   # version; head_dim 96 refused (size 0); empty batch
+
+
+def test_debug_set_wait_refuses_bad_stall(lib):
+    assert lib.mt_debug_set_wait(0, 2) == -1
+    assert lib.mt_debug_set_wait(0, 0) == 0

@@ -168,6 +168,28 @@ def test_bad_page_id_sets_status_without_fault():
         assert step.status()[0] == mt.MedusaTreeError(-4, "").status
 
 
+def test_bounded_wait_times_out_and_the_next_call_is_correct():
+    # The tensor-core kernel's first pipeline wait is made one that nothing
+    # completes, with a 200 us bound: the call must return, report
+    # MT_ERR_TIMEOUT in its status word and leave the context usable; the next
+    # call, with the default bound, must match the oracle.
+    spec = workloads.custom("timeout", B=3, Hq=8, Hkv=2, head_dim=128, dtype="bf16",
+                            prefix=("list", [300, 40, 1000]), tree=("fanout", (3, 2), 9), max_depth=2)
+    w = workloads.generate(spec, seed=0)
+    step = Step(w, kernel="tc")
+    try:
+        mt.debug_set_wait(200_000, stall=True)
+        step.attn()
+        assert step.status()[0] == -6
+    finally:
+        mt.debug_set_wait(0, stall=False)
+    step.attn()
+    assert step.status()[0] == 0
+    want = oracle.tree_attn(w)
+    got = step.out.float().cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - want)) <= 1e-2
+
+
 def test_bad_tree_sets_status_without_fault():
     spec = workloads.custom("badtree", B=2, Hq=4, Hkv=2, head_dim=128, dtype="f16",
                             prefix=("list", [10, 40]), tree=("fanout", (3, 2), 6), max_depth=2)
