@@ -15,9 +15,9 @@
 //              loads of page p of every tile (K and V, 128-byte swizzle, page
 //              ids from the block table; absent pages use an out-of-range row,
 //              which TMA fills with zeros).  A single issuing thread cannot
-//              keep HBM busy with 2 KB boxes; four can.  Producer 0 also loads
-//              each piece's rotated queries (one 128-row x 64-col box per M
-//              tile and half);
+//              keep HBM busy with 2 KB boxes; four can.  A piece's rotated
+//              queries go through the same ring, one slot per M tile ahead of
+//              the piece's tiles, their boxes shared out over the producers;
 //   QK issuer  one thread copies each piece's queries from shared memory into
 //              TMEM and issues S = Q K^T (M 128, N 64, K D; A = Q from TMEM)
 //              into TMEM, for M tile m as soon as the softmax has read S_m;
@@ -31,9 +31,9 @@
 //              to a 128-byte-swizzled shared-memory tile; at the end of a
 //              piece O / l goes to the output (whole segment) or O, m, l to a
 //              partial slot.
-// Shared memory holds Q staging (up to 64 KB), P (16 KB per M tile) and a
-// ring of 32 KB K/V stages; TMEM holds O (2 x 128 columns), S (2 x 64) and Q
-// (2 x 64 packed 16-bit pairs).
+// Shared memory holds P (16 KB per M tile) and a ring of 32 KB slots (a
+// tile's K and V, or an M tile's queries); TMEM holds O (2 x 128 columns),
+// S (2 x 64) and Q (2 x 64 packed 16-bit pairs).
 // Tensor-core instructions are issued by the elected lane of a converged warp
 // (tc::elect_one), which issues about twice as fast as a lane-0 branch.
 // Every mbarrier wait is bounded (2 s unless the caller set another limit);
@@ -61,15 +61,27 @@ __host__ __device__ constexpr int pow2_at_least(int x) {
 template <int D, int MT>
 struct Cfg {
   static constexpr int NH = D / 64;                     // 64-element halves of a head row
-  static constexpr int kQBytes = MT * NH * 128 * 128;   // [m][half][128 rows x 128 B]
+  // A piece's queries travel through the K/V ring: M tile m's 128 rows x D
+  // (the [half][128 rows x 128 B] boxes) fill one ring slot, which is exactly
+  // one stage (K and V of 64 keys), so no shared memory is set aside for them
+  // and the next piece's queries are prefetched in ring order.
   static constexpr int kPTile = 128 * kTileKeys * 2;     // P of one M tile: 128 rows x 128 B
-  static constexpr int kPBytes = MT * kPTile;            // [m]
+  // P buffers per M tile.  Two would let the softmax of tile t wait for the
+  // P.V of tile t - 2 instead of t - 1, but measured slower on every
+  // workload (serving 78.2 against 75.6 us at four stages, 84.8 against 76.8
+  // when it cost a stage), so there is one.
+  static constexpr int NPB = 1;
+  static constexpr int kPBytes = MT * NPB * kPTile;      // [m][buffer]
   static constexpr int kHalfTile = kTileKeys * 128;     // 64 keys x 128 B
   static constexpr int kStageBytes = 2 * NH * kHalfTile;  // K and V halves
   static constexpr int kBarBytes = 2048;  // barriers (first 1 KB) + the CTA's piece list
-  static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kQBytes - kPBytes) / kStageBytes;
-  static constexpr int STAGES = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kSmemBytes = 1024 + kQBytes + kPBytes + STAGES * kStageBytes + kBarBytes;
+  static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kPBytes) / kStageBytes;
+  // ring depth: two M tiles run best with four stages (more stages measured
+  // slower: the loads in flight then compete with the MMAs and P for shared
+  // memory bandwidth); one M tile streams faster with more
+  static constexpr int kStageCap = MT == 2 ? 4 : 8;
+  static constexpr int STAGES = kStagesFit > kStageCap ? kStageCap : kStagesFit;
+  static constexpr int kSmemBytes = 1024 + kPBytes + STAGES * kStageBytes + kBarBytes;
   static constexpr int kSoftmaxWarps = 4 * MT;
   static constexpr int kQkWarp = kSoftmaxWarps;
   static constexpr int kPvWarp = kSoftmaxWarps + 1;
@@ -148,20 +160,18 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sP = sQ + C::kQBytes;     // [m] P tiles, 128-byte swizzled, K-major
+  constexpr int NPB = C::NPB;
+  uint8_t* sP = smem;                // [m][buffer] P tiles, 128-byte swizzled, K-major
   uint8_t* sKV = sP + C::kPBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
-  uint64_t* full = bars;                // [S] K/V stage landed
-  uint64_t* empty = full + S;           // [S] K/V stage consumed by its P.V
+  uint64_t* full = bars;                // [S] ring slot landed (a tile's K/V, or an M tile's queries)
+  uint64_t* empty = full + S;           // [S] ring slot consumed (by its P.V, or its copy into TMEM)
   // per M tile, one phase per tile:
   uint64_t* s_full = empty + S;         // [MT] S computed
-  uint64_t* p_full = s_full + MT;       // [MT] P written (and O rescaled)
-  uint64_t* pv_done = p_full + MT;      // [MT] O += P V done
-  uint64_t* s_free = pv_done + MT;      // [MT] S read out by the softmax
-  uint64_t* q_full = s_free + MT;       // Q of the current piece landed
-  uint64_t* q_empty = q_full + 1;       // every Q K^T of the previous piece done
-  uint64_t* o_free = q_empty + 1;       // O of the previous piece read out
+  uint64_t* p_full = s_full + MT;       // [MT][NPB] P written (and O rescaled), one phase per use
+  uint64_t* pv_done = p_full + MT * NPB;  // [MT][NPB] O += P V done, one phase per use
+  uint64_t* s_free = pv_done + MT * NPB;  // [MT] S read out by the softmax
+  uint64_t* o_free = s_free + MT;       // O of the previous piece read out
   uint64_t* fin = o_free + 1;           // [2] every MMA of each issuer done
   uint64_t* never = fin + 2;            // nothing arrives here (timeout test hook)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
@@ -178,15 +188,15 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     }
     for (int m = 0; m < MT; ++m) {
       tc::mbar_init(&s_full[m], 1);
-      tc::mbar_init(&p_full[m], 4);
-      tc::mbar_init(&pv_done[m], 1);
+      for (int b = 0; b < NPB; ++b) {
+        tc::mbar_init(&p_full[m * NPB + b], 4);
+        tc::mbar_init(&pv_done[m * NPB + b], 1);
+      }
       tc::mbar_init(&s_free[m], 4);
     }
     tc::mbar_init(&fin[0], 1);
     tc::mbar_init(&fin[1], 1);
     tc::mbar_init(never, 1);
-    tc::mbar_init(q_full, 1);
-    tc::mbar_init(q_empty, 1);
     tc::mbar_init(o_free, C::kSoftmaxWarps);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -215,7 +225,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sQ_u = tc::smem_u32(sQ), sKV_u = tc::smem_u32(sKV), sP_u = tc::smem_u32(sP);
+  const uint32_t sKV_u = tc::smem_u32(sKV), sP_u = tc::smem_u32(sP);
   const uint64_t limit = a.wait_limit_ns;
 
   if (warp >= C::kProducer0) {
@@ -223,8 +233,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     // Each producer warp walks the schedule (page ids fetched warp-wide ahead
     // of use) and its lane 0 issues the K and V copies of its page of every
     // tile: one thread's TMA issue rate cannot keep up with HBM, four can.
-    // Producer 0 also loads each piece's queries once the previous piece's
-    // Q K^T are done, without holding back its K/V copies meanwhile.
+    // Each piece's queries take the ring's next MT slots before its tiles.
     const int pid = warp - C::kProducer0;
     const uint64_t policy = tc::policy_evict_first();
     const uint64_t q_policy = tc::policy_evict_last();
@@ -233,57 +242,48 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     pi.init(s_pieces, *s_npieces, a.sched, blockIdx.x, a.seq_lens);
     Piece pc;
     int pL = 0;
-    uint32_t it = 0, npieces = 0, nq = 0;
+    uint32_t pos = 0;  // ring position: MT query slots per piece, then one slot per tile
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       bool r = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
       ok = __all_sync(0xffffffffu, r) && ok;
     };
-    auto issue_q = [&]() {
-      if (lane == 0) {
-        tc::mbar_arrive_expect_tx(q_full, C::kQBytes);
-        for (int m = 0; m < MT; ++m) {
-          const int z = pc.b * a.T + (pc.rg * kTcRows + m * 128) / a.g;
-          for (int h = 0; h < C::NH; ++h)
-            tc::tma_load_3d(sQ + (m * C::NH + h) * (128 * 128), &tmap_q, h * 64, pc.kvh * a.g, z,
-                            q_full, q_policy);
-        }
-      }
-      ++nq;
-    };
     while (ok && pi.next(pc, pL)) {
-      bool q_pending = pid == 0;
-      if (q_pending && npieces == 0) {
-        issue_q();
-        q_pending = false;
+      // the piece's queries, one slot per M tile; the slot's boxes (one per
+      // 64-column half) are shared out over the producers, and every
+      // producer arrives once on every slot
+      for (int m = 0; m < MT && ok; ++m, ++pos) {
+        const uint32_t slot = pos % S;
+        if (pos >= (uint32_t)S) {
+          wait_all(&empty[slot], ((pos / S) - 1) & 1);
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          int mine = 0;
+          for (int h = 0; h < C::NH; ++h) mine += ((m * C::NH + h) % C::kProducers) == pid;
+          if (mine > 0) {
+            tc::mbar_arrive_expect_tx(&full[slot], (uint32_t)(mine * 128 * 128));
+            const int z = pc.b * a.T + (pc.rg * kTcRows + m * 128) / a.g;
+            for (int h = 0; h < C::NH; ++h)
+              if (((m * C::NH + h) % C::kProducers) == pid)
+                tc::tma_load_3d(sKV + slot * C::kStageBytes + h * (128 * 128), &tmap_q, h * 64, pc.kvh * a.g, z,
+                                &full[slot], q_policy);
+          } else {
+            tc::mbar_arrive(&full[slot]);
+          }
+        }
+        __syncwarp();
       }
-      const uint32_t it_first = it;
+      if (!ok) break;
       const int nkeys = pL + a.T;
       PageWindow pw;
       pw.init(a.block_tables + (size_t)pc.b * a.max_blocks, nkeys, a.max_blocks,
               pc.tile_begin * (kTileKeys / 16), lane);
-      for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
+      for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++pos) {
         const int y = pw.page(j * (kTileKeys / 16) + pid, lane);
-        const uint32_t stage = it % S;
-        if (q_pending) {
-          // the stage about to be refilled held a tile of this piece, whose
-          // P.V needs this piece's Q: load it now; otherwise only if the
-          // previous piece's Q K^T are already done
-          bool ready;
-          if (it >= (uint32_t)S && it - S >= it_first) {
-            wait_all(q_empty, (npieces - 1) & 1);
-            if (!ok) break;
-            ready = true;
-          } else {
-            ready = __shfl_sync(0xffffffffu, (int)tc::mbar_try_wait(q_empty, (npieces - 1) & 1), 0) != 0;
-          }
-          if (ready) {
-            issue_q();
-            q_pending = false;
-          }
-        }
-        if (it >= (uint32_t)S) {
-          wait_all(&empty[stage], ((it / S) - 1) & 1);
+        const uint32_t stage = pos % S;
+        if (pos >= (uint32_t)S) {
+          wait_all(&empty[stage], ((pos / S) - 1) & 1);
           if (!ok) break;
         }
         if (lane == 0) {
@@ -301,19 +301,11 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         }
         __syncwarp();
       }
-      if (!ok) break;
-      if (q_pending) {
-        wait_all(q_empty, (npieces - 1) & 1);
-        if (!ok) break;
-        issue_q();
-      }
-      ++npieces;
     }
     // no TMA load may still be writing shared memory when the CTA exits
     if (lane == 0) {
-      const uint32_t first = it > (uint32_t)S ? it - S : 0;
-      for (uint32_t t = first; t < it; ++t) drain_wait(&full[t % S], (t / S) & 1, a.status);
-      if (nq > 0) drain_wait(q_full, (nq - 1) & 1, a.status);
+      const uint32_t first = pos > (uint32_t)S ? pos - S : 0;
+      for (uint32_t t = first; t < pos; ++t) drain_wait(&full[t % S], (t / S) & 1, a.status);
     }
     __syncwarp();
   } else if (warp == C::kQkWarp) {
@@ -322,7 +314,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     pi.init(s_pieces, *s_npieces, a.sched, blockIdx.x, a.seq_lens);
     Piece pc;
     int pL = 0;
-    uint32_t it = 0, npieces = 0;
+    uint32_t it = 0, pos = 0;  // tiles so far; ring position (as the producers count it)
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       bool r = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
@@ -330,24 +322,27 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     };
     if (a.test_stall) wait_all(never, 0);  // test hook: a wait that can only time out
     while (ok && pi.next(pc, pL)) {
-      // the piece's queries: shared memory -> TMEM (after every Q K^T of the
-      // previous piece, in issue order), then the staging buffer is free
-      wait_all(q_full, npieces & 1);
+      // the piece's queries: ring slots -> TMEM (after every Q K^T of the
+      // previous piece, in issue order); each slot is free once copied
+      for (int m = 0; m < MT && ok; ++m) wait_all(&full[(pos + m) % S], ((pos + m) / S) & 1);
       if (!ok) break;
       tc::tc_fence_after();
-      for (int m = 0; m < MT; ++m)
+      for (int m = 0; m < MT; ++m) {
+        const uint32_t q_u = sKV_u + ((pos + m) % S) * C::kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t h = kk / 4, k4 = kk % 4;
           if (tc::elect_one())
             tc::tmem_cp_128x256b(tmem + C::q_col(m) + kk * 8,
-                                 tc::smem_desc(sQ_u + (m * C::NH + h) * (128 * 128) + k4 * 32, 16, 1024));
+                                 tc::smem_desc(q_u + h * (128 * 128) + k4 * 32, 16, 1024));
         }
-      if (tc::elect_one()) tc::mma_commit(q_empty);
+        if (tc::elect_one()) tc::mma_commit(&empty[(pos + m) % S]);
+      }
       __syncwarp();
-      for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
-        const uint32_t stage = it % S;
-        wait_all(&full[stage], (it / S) & 1);
+      pos += MT;
+      for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it, ++pos) {
+        const uint32_t stage = pos % S;
+        wait_all(&full[stage], (pos / S) & 1);
         if (!ok) break;
         const uint32_t k_u = sKV_u + stage * C::kStageBytes;
         // one descriptor per stage; a K slice is a constant offset (16-byte
@@ -375,7 +370,6 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         }
         if (!ok) break;
       }
-      ++npieces;
     }
     if (tc::elect_one()) tc::mma_commit(&fin[0]);
     __syncwarp();
@@ -387,7 +381,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     pi.init(s_pieces, *s_npieces, a.sched, blockIdx.x, a.seq_lens);
     Piece pc;
     int pL = 0;
-    uint32_t it = 0, npieces = 0;
+    uint32_t it = 0, npieces = 0, pos = 0;  // tiles, pieces, ring position
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       bool r = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
@@ -395,8 +389,9 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     };
     while (ok && pi.next(pc, pL)) {
       const int nkeys = pL + a.T;
-      for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it) {
-        const uint32_t stage = it % S;
+      pos += MT;  // the piece's query slots
+      for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++it, ++pos) {
+        const uint32_t stage = pos % S;
         const bool first = j == pc.tile_begin;
         if (first && npieces > 0) {
           wait_all(o_free, (npieces - 1) & 1);
@@ -406,7 +401,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         if (valid < kTileKeys) {
           // slots past the sequence hold stale data (possibly NaN): zero the V
           // rows so that 0-probability columns contribute exactly 0
-          wait_all(&full[stage], (it / S) & 1);
+          wait_all(&full[stage], (pos / S) & 1);
           if (!ok) break;
           uint8_t* vbase = sKV + stage * C::kStageBytes + C::NH * C::kHalfTile;
           const int nvec = (kTileKeys - valid) * 8;
@@ -418,11 +413,12 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         }
         const uint32_t v_u = sKV_u + stage * C::kStageBytes + C::NH * C::kHalfTile;
         for (int m = 0; m < MT; ++m) {
-          wait_all(&p_full[m], it & 1);
+          const int pb = (int)(it % NPB);
+          wait_all(&p_full[m * NPB + pb], (it / NPB) & 1);
           if (!ok) break;
           tc::tc_fence_after();
           const uint32_t d_t = tmem + C::o_col(m);
-          const uint32_t p_u = sP_u + m * C::kPTile;
+          const uint32_t p_u = sP_u + (m * NPB + pb) * C::kPTile;
           const uint64_t pd0 = tc::smem_desc(p_u, 16, 1024), vd0 = tc::smem_desc(v_u, C::kHalfTile, 1024);
           if (first) {
             if (tc::elect_one()) tc::mma_f16_ss<false>(d_t, pd0, vd0, kIdescPV);
@@ -432,7 +428,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
 #pragma unroll
           for (int kk = 1; kk < kTileKeys / 16; ++kk)  // next 16 keys: P +32 B, V +2048 B
             if (tc::elect_one()) tc::mma_f16_ss<true>(d_t, pd0 + (uint64_t)(kk * 2), vd0 + (uint64_t)(kk * 128), kIdescPV);
-          if (tc::elect_one()) tc::mma_commit(&pv_done[m]);
+          if (tc::elect_one()) tc::mma_commit(&pv_done[m * NPB + pb]);
           __syncwarp();
         }
         if (!ok) break;
@@ -534,15 +530,18 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
           rs1 += p1;
           pk[c] = Pack2<T>::pack(p0, p1);
         }
-        // P into this M tile's shared-memory buffer, once the P.V of tile
-        // it - 1 (which read it) is done: row r is 128 B (64 keys) in an
-        // 8-row, 128-byte swizzle atom (16-byte chunk c at c ^ (r % 8))
-        if (it >= 1) {
-          wait_all(&pv_done[m], (it - 1) & 1);
+        // P into buffer it % NPB of this M tile, once the P.V of tile it - NPB
+        // (which read it) is done: row r is 128 B (64 keys) in an 8-row,
+        // 128-byte swizzle atom (16-byte chunk c at c ^ (r % 8)).  A
+        // buffer's barriers complete once per use, and its next use needs
+        // this thread's P, so neither runs two phases ahead of these waits
+        const int pb = (int)(it % NPB);
+        if (it >= (uint32_t)NPB) {
+          wait_all(&pv_done[m * NPB + pb], ((it / NPB) - 1) & 1);
           if (!ok) break;
         }
         {
-          uint8_t* prow = sP + m * C::kPTile + (r >> 3) * 1024 + (r & 7) * 128;
+          uint8_t* prow = sP + (m * NPB + pb) * C::kPTile + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) =
@@ -550,7 +549,12 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
           tc::fence_proxy_async_smem();  // visible to the tensor core's reads
         }
         if (__any_sync(0xffffffffu, need_o)) {
-          // O holds the P.V sum up to tile it - 1 (done: waited above)
+          // O must hold the P.V sum up to tile it - 1 (with one buffer that
+          // P.V was waited for above)
+          if (NPB > 1) {
+            wait_all(&pv_done[m * NPB + (int)((it - 1) % NPB)], ((it - 1) / NPB) & 1);
+            if (!ok) break;
+          }
           tc::tc_fence_after();
 #pragma unroll 1
           for (int hh = 0; hh < D / 64; ++hh) {
@@ -567,11 +571,11 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         m_run = m_new;
         tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&p_full[m]);
+        if (lane == 0) tc::mbar_arrive(&p_full[m * NPB + pb]);
       }
       if (!ok) break;
-      // epilogue
-      wait_all(&pv_done[m], (it - 1) & 1);
+      // epilogue, once the piece's last P.V is done
+      wait_all(&pv_done[m * NPB + (int)((it - 1) % NPB)], ((it - 1) / NPB) & 1);
       if (!ok) break;
       tc::tc_fence_after();
       const int seg_row = m * 128 + r;
