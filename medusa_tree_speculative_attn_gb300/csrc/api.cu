@@ -256,9 +256,9 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   ap.piece_table = pp.piece_table;
   ap.wait_limit_ns = g_wait_limit_ns ? g_wait_limit_ns : 2000000000ull;
   ap.test_stall = g_wait_stall;
-  const bool prof = g_prof_n < g_prof_cap;
-  if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);
+  bool prof = g_prof_n < g_prof_cap;
   if (kernel == MT_KERNEL_SIMT) {
+    if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);
     st = cuda_status(launch_attn_simt(ap, Fp8Cache{fp8_cache(d), d->k_scale, d->v_scale}, d->dtype, stream));
   } else {
     alignas(64) unsigned char tmap_k[128], tmap_v[128], tmap_q[128];
@@ -267,10 +267,15 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
         make_cache_tmap(tmap_v, v_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
                         d->head_dim) != cudaSuccess ||
         make_q_tmap(tmap_q, ws + w.qrot, d->dtype, d->batch * d->tree_size, d->num_q_heads, ap.g,
-                    d->head_dim) != cudaSuccess)
+                    d->head_dim) != cudaSuccess) {
       st = MT_ERR_CUDA;
-    else
+      prof = false;
+    } else {
+      // the start event goes in after the descriptors are encoded, so that
+      // host time spent on them stays out of the kernel's window
+      if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);
       st = cuda_status(launch_attn_tc(ap, d->dtype, tmap_k, tmap_v, tmap_q, stream));
+    }
   }
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n++ + 1], stream);
   if (st != MT_OK) return st;

@@ -41,6 +41,7 @@
 // out, waits for its own TMA loads and MMAs, frees TMEM and returns.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "kernels.cuh"
@@ -51,6 +52,7 @@ namespace mt {
 namespace {
 
 constexpr int kSmemLimit = 232448;  // opt-in dynamic shared memory per CTA
+constexpr int kMaxDevices = 64;
 
 __host__ __device__ constexpr int pow2_at_least(int x) {
   int p = 32;
@@ -627,9 +629,17 @@ template <typename T, int D, int MT>
 cudaError_t launch_t(const AttnParams& a, const CUtensorMap* tk, const CUtensorMap* tv,
                      const CUtensorMap* tq, cudaStream_t stream) {
   using C = Cfg<D, MT>;
-  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<T, D, MT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // the shared-memory opt-in, once per kernel instance and device (outside
+  // the hot path of later calls)
+  static std::atomic<bool> opted[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !opted[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<T, D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) opted[dev].store(true, std::memory_order_release);
+  }
   return launch_pdl(attn_tc_kernel<T, D, MT>, dim3(a.sched.G), dim3(C::kThreads), (size_t)C::kSmemBytes, stream,
                     *tk, *tv, *tq, a);
 }
