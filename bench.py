@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one")
+    ap.add_argument("--cache", default="act", choices=["act", "e4m3"],
+                    help="KV cache elements: the act dtype, or FP8 E4M3 codes of value / scale")
     ap.add_argument("--sustain-s", type=float, default=1.0,
                     help="seconds of back-to-back replayed steps after the timed ones (0: skip)")
     ap.add_argument("--accept", default="fused", choices=["fused", "separate", "typical"],
@@ -232,14 +234,16 @@ def measure_candidates(w: dict, K: int, flush, stream, peak: float) -> dict:
             "heads": heads, "status": st, "l2": "flushed before each call", "launch": "CUDA graph replay"}
 
 
-def algorithmic_bytes(w_host: dict) -> dict:
-    """Bytes the path must move at least once (per step)."""
+def algorithmic_bytes(w_host: dict, cache_bytes=None) -> dict:
+    """Bytes the path must move at least once (per step); cache_bytes is the
+    size of a cached element (the act dtype's unless the cache is FP8)."""
     es = {"f32": 4, "f16": 2, "bf16": 2}[w_host["dtype"]]
+    cs = es if cache_bytes is None else cache_bytes
     B, T, Hq, Hkv, D = w_host["B"], w_host["T"], w_host["Hq"], w_host["Hkv"], w_host["head_dim"]
     L = np.asarray(w_host["seq_lens_host"] if "seq_lens_host" in w_host else w_host["seq_lens"], np.int64)
-    prefix_kv = int(L.sum()) * Hkv * D * 2 * es
+    prefix_kv = int(L.sum()) * Hkv * D * 2 * cs
     tree_qo = B * T * Hq * D * 2 * es              # q read, out written
-    tree_kv = B * T * Hkv * D * 2 * es             # the tree's own K/V
+    tree_kv = B * T * Hkv * D * 2 * cs             # the tree's own K/V, as cached
     attn = prefix_kv + tree_qo + tree_kv
     logits = 0
     if "vocab" in w_host:
@@ -260,10 +264,19 @@ def run_ours(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     w = workloads.generate(args.workload, seed=rank_seed(args.seed, rank), backend="torch", device=str(dev))
     spec = w["spec"]
+    k_scale = v_scale = 1.0
+    if args.cache == "e4m3":
+        # E4M3 codes of the N(0,1) caches / an amax-style scale (the largest
+        # |value| of the draws maps near 448); unused slots stay NaN codes
+        k_scale = float(w["k_cache"].float().nan_to_num(0.0).abs().max()) / 448.0
+        v_scale = float(w["v_cache"].float().nan_to_num(0.0).abs().max()) / 448.0
+        w["k_cache"] = (w["k_cache"].float() / k_scale).to(torch.float8_e4m3fn)
+        w["v_cache"] = (w["v_cache"].float() / v_scale).to(torch.float8_e4m3fn)
     B, T, md = w["B"], w["T"], w["max_depth"]
     stream = torch.cuda.current_stream()
     rope = mt.Rope(w["rope_base"], w["head_dim"], int(w["seq_lens_host"].max()) + T + 1)
-    desc = mt.make_desc(w["q"], w["k_cache"], w["block_tables"], args.splits, args.kernel)
+    desc = mt.make_desc(w["q"], w["k_cache"], w["block_tables"], args.splits, args.kernel,
+                        k_scale=k_scale, v_scale=v_scale)
     ws = mt.alloc_attn_workspace(desc, dev)
     aws = mt.alloc_accept_workspace(B, T, dev)
     out = torch.empty_like(w["q"])
@@ -286,7 +299,8 @@ def run_ours(args, rank, world, local_rank):
         s = src or w
         mt.tree_attn_paged(s["q"], w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"],
                            s["tree_parents"], s["tree_depths"], out, k_new=s["k_new"], v_new=s["v_new"],
-                           rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel)
+                           rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel,
+                           k_scale=k_scale, v_scale=v_scale)
         if has_accept and args.accept == "fused":
             mt.tree_accept_commit(s["tree_tokens"], s["logits"], s["tree_parents"], alen, path,
                                   w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"], rel,
@@ -323,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
         e0.record(stream)
         mt.tree_attn_paged(w["q"], w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"],
                            w["tree_parents"], w["tree_depths"], out, k_new=w["k_new"], v_new=w["v_new"],
-                           rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel)
+                           rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel,
+                           k_scale=k_scale, v_scale=v_scale)
         e1.record(stream)
         if has_accept:
             mt.tree_accept_greedy(w["tree_tokens"], w["logits"], w["tree_parents"], alen, path,
@@ -478,7 +493,7 @@ def run_ours(args, rank, world, local_rank):
         e2e = {"value": whole_job_rate(B * T, world, e2e_ms), "unit": UNIT, "ms_per_step": e2e_ms,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
-    ab = algorithmic_bytes(w)
+    ab = algorithmic_bytes(w, 1 if args.cache == "e4m3" else None)
     peak, peak_src = measured_peaks()
     cand = measure_candidates(w, K, flush, stream, peak) if has_accept else None
     main_avg = float(np.mean(main_ms)) if main_ms else None
@@ -505,6 +520,8 @@ def run_ours(args, rank, world, local_rank):
                    "prefix": list(spec.prefix), "logits": (f"{w['logits_dtype']} vocab {w['vocab']}"
                                                            if has_accept else None),
                    "kernel": args.kernel, "num_splits": args.splits, "accept": args.accept,
+                   "kv_cache": "act dtype" if args.cache == "act" else
+                   f"fp8 e4m3 codes (k_scale {k_scale:.5g}, v_scale {v_scale:.5g})",
                    "launch": "one CUDA graph per step" if graph is not None else "kernel by kernel",
                    "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
         "kv_gbs": ab["prefix_kv"] / (main_avg * 1e-3) / 1e9 if main_avg else None,
@@ -515,7 +532,7 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": K * (3 + (0 if not has_accept else 1 if args.accept == "fused" else 2)),
         "wall_s_timed_region": wall,
     }
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and args.cache == "act":
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_budget_s)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -115,10 +115,12 @@ typedef struct {
    * scale, the tree's own K/V included: mt_tree_attn_paged writes the code of
    * (act-rounded rotated key or raw value) / scale, divided in fp32 and
    * rounded to nearest even with saturation to +-448, and reads every visible
-   * slot back through the scale.  Runs on the SIMT kernel (MT_KERNEL_TC is
-   * unsupported with it); mt_kv_commit and mt_tree_accept_commit move the
-   * 1-byte elements.  k_scale, v_scale: positive and finite for MT_E4M3,
-   * ignored otherwise. */
+   * slot back through the scale.  Runs on either kernel: the tensor-core
+   * kernel (fp16/bf16 dtype) loads the codes with TMA, converts them exactly
+   * to the act dtype in shared memory, and applies k_scale with the softmax
+   * scale and v_scale to the output; MT_KERNEL_AUTO picks it as for a 16-bit
+   * cache.  mt_kv_commit and mt_tree_accept_commit move the 1-byte elements.
+   * k_scale, v_scale: positive and finite for MT_E4M3, ignored otherwise. */
   int cache_dtype;
   float k_scale;
   float v_scale;

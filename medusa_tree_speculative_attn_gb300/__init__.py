@@ -210,7 +210,8 @@ def tree_attn_paged(q, k_cache, v_cache, block_tables, seq_lens, tree_parents, t
     """out[b,i,h] = attention of tree node i (head h) over the prefix + its ancestors.
 
     The caches hold q's dtype, or FP8 E4M3 codes (torch.float8_e4m3fn) of
-    value / k_scale and value / v_scale, read on the CUDA-core kernel."""
+    value / k_scale and value / v_scale (read on either kernel; the tensor-core
+    kernel converts the codes to q's dtype in shared memory)."""
     for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("out", out)):
         _need(t, name, q.dtype, 4)
     cache_dtype = torch.float8_e4m3fn if _fp8(k_cache) else q.dtype

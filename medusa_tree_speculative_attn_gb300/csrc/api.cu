@@ -43,9 +43,10 @@ bool fp8_cache(const mt_attn_desc* d) { return d->cache_dtype == MT_E4M3; }
 // Bytes of one cache element.
 int cache_elem_bytes(const mt_attn_desc* d) { return fp8_cache(d) ? 1 : elem_bytes(d->dtype); }
 
-// Which attention kernel a descriptor runs.
+// Which attention kernel a descriptor runs (an FP8 cache included: the
+// tensor-core kernel converts its codes to the act dtype in shared memory).
 int select_kernel(const mt_attn_desc* d) {
-  if (d->kernel == MT_KERNEL_SIMT || fp8_cache(d)) return MT_KERNEL_SIMT;
+  if (d->kernel == MT_KERNEL_SIMT) return MT_KERNEL_SIMT;
   if (d->kernel == MT_KERNEL_TC) return MT_KERNEL_TC;
   if (d->dtype == MT_F32) return MT_KERNEL_SIMT;
   return tc_supported(d->head_dim, d->num_q_heads / d->num_kv_heads) ? MT_KERNEL_TC : MT_KERNEL_SIMT;
@@ -119,7 +120,6 @@ int check_desc(const mt_attn_desc* d) {
   if (fp8_cache(d)) {
     if (!(d->k_scale > 0.f) || std::isinf(d->k_scale) || !(d->v_scale > 0.f) || std::isinf(d->v_scale))
       return MT_ERR_INVALID_ARG;
-    if (d->kernel == MT_KERNEL_TC) return MT_ERR_UNSUPPORTED;
   }
   return MT_OK;
 }
@@ -262,10 +262,21 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
     st = cuda_status(launch_attn_simt(ap, Fp8Cache{fp8_cache(d), d->k_scale, d->v_scale}, d->dtype, stream));
   } else {
     alignas(64) unsigned char tmap_k[128], tmap_v[128], tmap_q[128];
-    if (make_cache_tmap(tmap_k, k_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
-                        d->head_dim) != cudaSuccess ||
-        make_cache_tmap(tmap_v, v_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size,
-                        d->head_dim) != cudaSuccess ||
+    const bool f8 = fp8_cache(d);
+    cudaError_t ek, ev;
+    if (f8) {
+      ek = make_cache_tmap_e4m3(tmap_k, k_cache, d->num_pages, d->num_kv_heads, d->page_size, d->head_dim);
+      ev = make_cache_tmap_e4m3(tmap_v, v_cache, d->num_pages, d->num_kv_heads, d->page_size, d->head_dim);
+    } else {
+      ek = make_cache_tmap(tmap_k, k_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size, d->head_dim);
+      ev = make_cache_tmap(tmap_v, v_cache, d->dtype, d->num_pages, d->num_kv_heads, d->page_size, d->head_dim);
+    }
+    // an FP8 cache: the K scale joins the softmax scale, the V scale the output
+    AttnParams apt = ap;
+    apt.cache_fp8 = f8 ? 1 : 0;
+    apt.v_scale = f8 ? d->v_scale : 1.f;
+    if (f8) apt.scale_log2 = (float)((double)ap.scale_log2 * (double)d->k_scale);
+    if (ek != cudaSuccess || ev != cudaSuccess ||
         make_q_tmap(tmap_q, ws + w.qrot, d->dtype, d->batch * d->tree_size, d->num_q_heads, ap.g,
                     d->head_dim) != cudaSuccess) {
       st = MT_ERR_CUDA;
@@ -274,7 +285,7 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
       // the start event goes in after the descriptors are encoded, so that
       // host time spent on them stays out of the kernel's window
       if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n], stream);
-      st = cuda_status(launch_attn_tc(ap, d->dtype, tmap_k, tmap_v, tmap_q, stream));
+      st = cuda_status(launch_attn_tc(apt, d->dtype, tmap_k, tmap_v, tmap_q, stream));
     }
   }
   if (prof) cudaEventRecord(g_prof_ev[2 * g_prof_n++ + 1], stream);

@@ -60,7 +60,7 @@ __host__ __device__ constexpr int pow2_at_least(int x) {
   return p;
 }
 
-template <int D, int MT>
+template <int D, int MT, bool FP8 = false>
 struct Cfg {
   static constexpr int NH = D / 64;                     // 64-element halves of a head row
   // A piece's queries travel through the K/V ring: M tile m's 128 rows x D
@@ -77,13 +77,19 @@ struct Cfg {
   static constexpr int kHalfTile = kTileKeys * 128;     // 64 keys x 128 B
   static constexpr int kStageBytes = 2 * NH * kHalfTile;  // K and V halves
   static constexpr int kBarBytes = 2048;  // barriers (first 1 KB) + the CTA's piece list
-  static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kPBytes) / kStageBytes;
+  // An FP8 (E4M3) cache: each producer TMAs its page's codes (K then V,
+  // 16 rows x D bytes each) into a private ring of kF8Depth slots and converts
+  // them into the ring stage the MMAs read.
+  static constexpr int kF8Depth = 4;
+  static constexpr int kF8PageBytes = 2 * 16 * D;
+  static constexpr int kF8Bytes = FP8 ? (kTileKeys / 16) * kF8Depth * kF8PageBytes : 0;
+  static constexpr int kStagesFit = (kSmemLimit - 1024 - kBarBytes - kPBytes - kF8Bytes) / kStageBytes;
   // ring depth: two M tiles run best with four stages (more stages measured
   // slower: the loads in flight then compete with the MMAs and P for shared
   // memory bandwidth); one M tile streams faster with more
   static constexpr int kStageCap = MT == 2 ? 4 : 8;
   static constexpr int STAGES = kStagesFit > kStageCap ? kStageCap : kStagesFit;
-  static constexpr int kSmemBytes = 1024 + kPBytes + STAGES * kStageBytes + kBarBytes;
+  static constexpr int kSmemBytes = 1024 + kPBytes + STAGES * kStageBytes + kF8Bytes + kBarBytes;
   static constexpr int kSoftmaxWarps = 4 * MT;
   static constexpr int kQkWarp = kSoftmaxWarps;
   static constexpr int kPvWarp = kSoftmaxWarps + 1;
@@ -123,6 +129,31 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Eight E4M3 codes (8 bytes, first element lowest) as eight act-dtype values
+// (16 bytes).  Every E4M3 value is exact in fp16, fp32 and bf16: codes go
+// pairwise to f16x2, and for bf16 on through fp32.
+template <typename T>
+__device__ __forceinline__ uint4 e4m3x8_to_act(uint2 c8) {
+  uint32_t h[4];
+  const uint32_t w[2] = {c8.x, c8.y};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint16_t pair = (uint16_t)(w[i / 2] >> (16 * (i % 2)));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h[i]) : "h"(pair));
+  }
+  if (std::is_same<T, __nv_bfloat16>::value) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 x;
+      memcpy(&x, &h[i], 4);
+      const float2 f = __half22float2(x);
+      __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+      memcpy(&h[i], &b, 4);
+    }
+  }
+  return make_uint4(h[0], h[1], h[2], h[3]);
+}
+
 // Bounded wait that ignores the abort flag (used to drain in-flight work).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* status) {
   const uint64_t t0 = tc::global_timer_ns();
@@ -148,12 +179,12 @@ __device__ __forceinline__ unsigned long long tile_visibility(int L, int k0,
   return pre | tree;
 }
 
-template <typename T, int D, int MT>
-__global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
+template <typename T, int D, int MT, bool FP8>
+__global__ void __launch_bounds__(Cfg<D, MT, FP8>::kThreads, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmap_k,
                    const __grid_constant__ CUtensorMap tmap_v,
                    const __grid_constant__ CUtensorMap tmap_q, const AttnParams a) {
-  using C = Cfg<D, MT>;
+  using C = Cfg<D, MT, FP8>;
   constexpr int S = C::STAGES;
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   constexpr uint32_t kIdescQK = tc::idesc_f16(kBf16, false, 128, kTileKeys);
@@ -165,7 +196,8 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   constexpr int NPB = C::NPB;
   uint8_t* sP = smem;                // [m][buffer] P tiles, 128-byte swizzled, K-major
   uint8_t* sKV = sP + C::kPBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + S * C::kStageBytes);
+  uint8_t* sF8 = sKV + S * C::kStageBytes;  // [producer][kF8Depth] FP8 code pages (FP8 caches)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sF8 + C::kF8Bytes);
   uint64_t* full = bars;                // [S] ring slot landed (a tile's K/V, or an M tile's queries)
   uint64_t* empty = full + S;           // [S] ring slot consumed (by its P.V, or its copy into TMEM)
   // per M tile, one phase per tile:
@@ -176,9 +208,13 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   uint64_t* o_free = s_free + MT;       // O of the previous piece read out
   uint64_t* fin = o_free + 1;           // [2] every MMA of each issuer done
   uint64_t* never = fin + 2;            // nothing arrives here (timeout test hook)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  uint64_t* f8_full = never + 1;        // [producer][kF8Depth] FP8 code page landed (FP8 caches)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(f8_full + C::kProducers * C::kF8Depth);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_npieces = const_cast<int*>(abort_flag + 1);
+  uint32_t* s_f8pos = reinterpret_cast<uint32_t*>(s_npieces + 1);  // [producer][kF8Depth] ring positions
+  static_assert((2 * 8 + 8 * 2 + 6 + C::kProducers * C::kF8Depth) * 8 + 12 +
+                    C::kProducers * C::kF8Depth * 4 <= 1024, "barrier area");
   PieceRec* s_pieces = reinterpret_cast<PieceRec*>(reinterpret_cast<uint8_t*>(bars) + 1024);
   static_assert(kMaxPieceRecs * sizeof(PieceRec) <= C::kBarBytes - 1024, "piece list");
 
@@ -199,6 +235,7 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
     tc::mbar_init(&fin[0], 1);
     tc::mbar_init(&fin[1], 1);
     tc::mbar_init(never, 1);
+    for (int k = 0; k < C::kProducers * C::kF8Depth; ++k) tc::mbar_init(&f8_full[k], 1);
     tc::mbar_init(o_free, C::kSoftmaxWarps);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -250,16 +287,71 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       bool r = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
       ok = __all_sync(0xffffffffu, r) && ok;
     };
+    // FP8 caches: tiles whose codes were issued (f8_issued) and converted
+    // into their stages (f8_done); slot f of this producer's FP8 ring holds
+    // the codes of tile f8_done + ((f - f8_done) mod depth), whose ring
+    // position is in s_f8pos.
+    uint32_t f8_issued = 0, f8_done = 0;
+    unsigned long long q_slots = 0;  // bit p % 64: ring position p held queries (FP8 drain)
+    // Convert the oldest issued tile: wait for its codes and for its stage,
+    // then each lane turns half a row (D/2 codes of K, then of V) into act
+    // values in the stage's 128-byte-swizzled layout (row pid * 16 + r), and
+    // the warp arrives on the stage's barrier (all four producers do).
+    auto f8_convert_oldest = [&]() {
+      const uint32_t f = f8_done % C::kF8Depth;
+      wait_all(&f8_full[pid * C::kF8Depth + f], (f8_done / C::kF8Depth) & 1);
+      if (!ok) return;
+      const uint32_t p = s_f8pos[pid * C::kF8Depth + f];
+      const uint32_t st = p % S;
+      if (p >= (uint32_t)S) {
+        wait_all(&empty[st], ((p / S) - 1) & 1);
+        if (!ok) return;
+      }
+      const uint8_t* codes = sF8 + (pid * C::kF8Depth + f) * C::kF8PageBytes;
+      // 16-byte chunks of codes: consecutive lanes read consecutive chunks
+      // (no bank conflicts); chunk q is row q / (D/16), columns 16 (q % (D/16))
+      // on, and becomes two 8-column chunks of the stage's row pid * 16 + row
+      constexpr int kChunksPerRow = D / 16;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        uint8_t* dst = sKV + st * C::kStageBytes + kv * C::NH * C::kHalfTile;
+#pragma unroll
+        for (int i = 0; i < 16 * kChunksPerRow / 32; ++i) {
+          const int q = i * 32 + lane;
+          const int r = q / kChunksPerRow, col = (q % kChunksPerRow) * 16;
+          const uint4 c16 = *reinterpret_cast<const uint4*>(codes + kv * 16 * D + q * 16);
+          const int row = pid * 16 + r;
+          uint8_t* drow = dst + (col / 64) * C::kHalfTile + row * 128;
+          const int c0 = (col % 64) / 8;
+          *reinterpret_cast<uint4*>(drow + ((c0 ^ (row & 7)) << 4)) = e4m3x8_to_act<T>(make_uint2(c16.x, c16.y));
+          *reinterpret_cast<uint4*>(drow + (((c0 + 1) ^ (row & 7)) << 4)) =
+              e4m3x8_to_act<T>(make_uint2(c16.z, c16.w));
+        }
+      }
+      tc::fence_proxy_async_smem();  // the stage is read by the tensor core; the codes' slot is refilled by TMA
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&full[st]);
+      ++f8_done;
+    };
+    // convert every issued tile at ring position <= p - S, before a wait on
+    // position p's stage (which can depend on them)
+    auto f8_flush_until = [&](uint32_t p) {
+      while (ok && f8_done < f8_issued && p >= (uint32_t)S &&
+             s_f8pos[pid * C::kF8Depth + f8_done % C::kF8Depth] <= p - S)
+        f8_convert_oldest();
+    };
     while (ok && pi.next(pc, pL)) {
       // the piece's queries, one slot per M tile; the slot's boxes (one per
       // 64-column half) are shared out over the producers, and every
       // producer arrives once on every slot
       for (int m = 0; m < MT && ok; ++m, ++pos) {
         const uint32_t slot = pos % S;
-        if (pos >= (uint32_t)S) {
+        if (FP8) f8_flush_until(pos);
+        if (pos >= (uint32_t)S && ok) {
           wait_all(&empty[slot], ((pos / S) - 1) & 1);
           if (!ok) break;
         }
+        q_slots |= 1ull << (pos % 64);
         if (lane == 0) {
           int mine = 0;
           for (int h = 0; h < C::NH; ++h) mine += ((m * C::NH + h) % C::kProducers) == pid;
@@ -284,6 +376,28 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       for (int j = pc.tile_begin; j < pc.tile_end; ++j, ++pos) {
         const int y = pw.page(j * (kTileKeys / 16) + pid, lane);
         const uint32_t stage = pos % S;
+        if (FP8) {
+          // the codes go to this producer's FP8 ring; converting them into
+          // the stage waits for the stage, later
+          if (f8_issued - f8_done == (uint32_t)C::kF8Depth) f8_convert_oldest();
+          if (!ok) break;
+          q_slots &= ~(1ull << (pos % 64));
+          const uint32_t f = f8_issued % C::kF8Depth;
+          if (lane == 0) {
+            uint64_t* bar = &f8_full[pid * C::kF8Depth + f];
+            tc::mbar_arrive_expect_tx(bar, C::kF8PageBytes);
+            uint8_t* kdst = sF8 + (pid * C::kF8Depth + f) * C::kF8PageBytes;
+            int row = oob_row;
+            if (y >= 0 && y < a.num_pages) row = (y * a.Hkv + pc.kvh) * 16;
+            else if (j * kTileKeys + pid * 16 < nkeys) set_status(a.status, kStPages);
+            tc::tma_load_2d(kdst, &tmap_k, 0, row, bar, policy);
+            tc::tma_load_2d(kdst + 16 * D, &tmap_v, 0, row, bar, policy);
+            s_f8pos[pid * C::kF8Depth + f] = pos;
+          }
+          __syncwarp();
+          ++f8_issued;
+          continue;
+        }
         if (pos >= (uint32_t)S) {
           wait_all(&empty[stage], ((pos / S) - 1) & 1);
           if (!ok) break;
@@ -304,10 +418,20 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
         __syncwarp();
       }
     }
+    if (FP8)
+      while (ok && f8_done < f8_issued) f8_convert_oldest();
     // no TMA load may still be writing shared memory when the CTA exits
     if (lane == 0) {
+      if (FP8) {
+        // codes never converted (after an abort), then the query slots
+        for (uint32_t u = f8_done; u < f8_issued; ++u)
+          drain_wait(&f8_full[pid * C::kF8Depth + u % C::kF8Depth], (u / C::kF8Depth) & 1, a.status);
+      }
+      // the last S positions' loads (with FP8 codes, only query slots are
+      // loaded into stages by TMA; the rest were written by the warps)
       const uint32_t first = pos > (uint32_t)S ? pos - S : 0;
-      for (uint32_t t = first; t < pos; ++t) drain_wait(&full[t % S], (t / S) & 1, a.status);
+      for (uint32_t t = first; t < pos; ++t)
+        if (!FP8 || ((q_slots >> (t % 64)) & 1ull)) drain_wait(&full[t % S], (t / S) & 1, a.status);
     }
     __syncwarp();
   } else if (warp == C::kQkWarp) {
@@ -581,7 +705,9 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
       if (!ok) break;
       tc::tc_fence_after();
       const int seg_row = m * 128 + r;
-      const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+      // an FP8 cache's V scale multiplies the output (direct) or the partial O
+      const float vs = FP8 ? a.v_scale : 1.f;
+      const float inv = (l_run > 0.f ? 1.f / l_run : 0.f) * vs;
 #pragma unroll 1
       for (int hh = 0; hh < D / 64; ++hh) {
         uint32_t o[64];
@@ -606,8 +732,8 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 16; ++c)
               dst[(size_t)c * a.part_rows] =
-                  make_float4(__uint_as_float(o[4 * c]), __uint_as_float(o[4 * c + 1]),
-                              __uint_as_float(o[4 * c + 2]), __uint_as_float(o[4 * c + 3]));
+                  make_float4(__uint_as_float(o[4 * c]) * vs, __uint_as_float(o[4 * c + 1]) * vs,
+                              __uint_as_float(o[4 * c + 2]) * vs, __uint_as_float(o[4 * c + 3]) * vs);
           }
         }
       }
@@ -625,10 +751,10 @@ __global__ void __launch_bounds__(Cfg<D, MT>::kThreads, 1)
   if (warp == C::kQkWarp) tc::tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <typename T, int D, int MT>
+template <typename T, int D, int MT, bool FP8>
 cudaError_t launch_t(const AttnParams& a, const CUtensorMap* tk, const CUtensorMap* tv,
                      const CUtensorMap* tq, cudaStream_t stream) {
-  using C = Cfg<D, MT>;
+  using C = Cfg<D, MT, FP8>;
   // the shared-memory opt-in, once per kernel instance and device (outside
   // the hot path of later calls)
   static std::atomic<bool> opted[kMaxDevices];
@@ -636,21 +762,22 @@ cudaError_t launch_t(const AttnParams& a, const CUtensorMap* tk, const CUtensorM
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !opted[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<T, D, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    e = cudaFuncSetAttribute(attn_tc_kernel<T, D, MT, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted[dev].store(true, std::memory_order_release);
   }
-  return launch_pdl(attn_tc_kernel<T, D, MT>, dim3(a.sched.G), dim3(C::kThreads), (size_t)C::kSmemBytes, stream,
-                    *tk, *tv, *tq, a);
+  return launch_pdl(attn_tc_kernel<T, D, MT, FP8>, dim3(a.sched.G), dim3(C::kThreads), (size_t)C::kSmemBytes,
+                    stream, *tk, *tv, *tq, a);
 }
 
-template <typename T>
+template <typename T, bool FP8>
 cudaError_t launch_dtype(const AttnParams& a, const CUtensorMap* tk, const CUtensorMap* tv,
                          const CUtensorMap* tq, cudaStream_t stream) {
   const bool one = a.rows <= 128;
   if (a.D == 64)
-    return one ? launch_t<T, 64, 1>(a, tk, tv, tq, stream) : launch_t<T, 64, 2>(a, tk, tv, tq, stream);
-  return one ? launch_t<T, 128, 1>(a, tk, tv, tq, stream) : launch_t<T, 128, 2>(a, tk, tv, tq, stream);
+    return one ? launch_t<T, 64, 1, FP8>(a, tk, tv, tq, stream) : launch_t<T, 64, 2, FP8>(a, tk, tv, tq, stream);
+  return one ? launch_t<T, 128, 1, FP8>(a, tk, tv, tq, stream) : launch_t<T, 128, 2, FP8>(a, tk, tv, tq, stream);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -688,6 +815,24 @@ cudaError_t make_cache_tmap(void* map_out, const void* base, int dtype, int num_
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// An FP8 (E4M3) paged cache [num_pages][Hkv][16][D] of 1-byte codes as a 2-D
+// tensor of num_pages*Hkv*16 rows by D columns; boxes of 16 rows (one page of
+// one KV head) by D columns, no swizzle (the producers convert the codes into
+// the swizzled stage), zero fill outside.
+cudaError_t make_cache_tmap_e4m3(void* map_out, const void* base, int num_pages, int Hkv, int P, int D) {
+  CUtensorMap* map = static_cast<CUtensorMap*>(map_out);
+  auto enc = get_encode();
+  if (!enc) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)num_pages * Hkv * P};
+  cuuint64_t strides[1] = {(cuuint64_t)D};
+  cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)P};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // The rotated queries [B*T][Hq][D] as a 3-D tensor (D, Hq, B*T); a box of 64
 // columns x g heads x 128/g nodes is one 128-row M tile half (row = node * g +
 // head in group), 128-byte swizzle.  Rows past the last node read zeros.
@@ -713,8 +858,12 @@ cudaError_t launch_attn_tc(const AttnParams& a, int dtype, const void* tmap_k, c
   const CUtensorMap* tk = static_cast<const CUtensorMap*>(tmap_k);
   const CUtensorMap* tv = static_cast<const CUtensorMap*>(tmap_v);
   const CUtensorMap* tq = static_cast<const CUtensorMap*>(tmap_q);
-  if (dtype == 1) return launch_dtype<__half>(a, tk, tv, tq, stream);
-  return launch_dtype<__nv_bfloat16>(a, tk, tv, tq, stream);
+  if (a.cache_fp8) {
+    if (dtype == 1) return launch_dtype<__half, true>(a, tk, tv, tq, stream);
+    return launch_dtype<__nv_bfloat16, true>(a, tk, tv, tq, stream);
+  }
+  if (dtype == 1) return launch_dtype<__half, false>(a, tk, tv, tq, stream);
+  return launch_dtype<__nv_bfloat16, false>(a, tk, tv, tq, stream);
 }
 
 }  // namespace mt

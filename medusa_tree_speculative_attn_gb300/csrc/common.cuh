@@ -222,6 +222,8 @@ struct AttnParams {
   const int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs] (tensor-core kernel)
   unsigned long long wait_limit_ns;  // bound of every pipeline wait (tensor-core kernel)
   int test_stall;                    // tensor-core kernel: first wait on a barrier nothing completes
+  int cache_fp8;                     // tensor-core kernel: the caches hold E4M3 codes of value / scale
+  float v_scale;                     // their V scale (the K scale is folded into scale_log2)
 };
 
 // A CTA's pieces, listed ahead of time by the prep kernel (up to

@@ -109,7 +109,8 @@ constexpr int kTcRows = 256;
 constexpr int kTcCtasPerSm = 1;
 
 cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream);
-// An FP8 (E4M3) KV cache: codes of value / scale, read by the CUDA-core kernel only.
+// An FP8 (E4M3) KV cache for the CUDA-core kernel: codes of value / scale (the
+// tensor-core kernel takes the same facts through AttnParams).
 struct Fp8Cache {
   int on;
   float k_scale, v_scale;
@@ -121,6 +122,7 @@ cudaError_t launch_attn_simt(const AttnParams& a, const Fp8Cache& f8, int dtype,
 cudaError_t make_cache_tmap(void* map_out, const void* base, int dtype, int num_pages, int Hkv,
                             int P, int D);
 cudaError_t make_q_tmap(void* map_out, const void* base, int dtype, int BT, int Hq, int g, int D);
+cudaError_t make_cache_tmap_e4m3(void* map_out, const void* base, int num_pages, int Hkv, int P, int D);
 // Whether the tensor-core kernel supports a configuration.
 bool tc_supported(int D, int g);
 cudaError_t launch_attn_tc(const AttnParams& a, int dtype, const void* tmap_k, const void* tmap_v,

@@ -49,29 +49,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Non-blocking test of four barriers at once (one round trip): whether the
-// phases with the given parity of bars[0..3] have all completed.
-__device__ __forceinline__ bool mbar_test_wait4(uint64_t* bars, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n"
-      ".reg .pred p0, p1, p2, p3;\n"
-      "mbarrier.test_wait.parity.shared::cta.b64 p0, [%1], %5;\n"
-      "mbarrier.test_wait.parity.shared::cta.b64 p1, [%2], %5;\n"
-      "mbarrier.test_wait.parity.shared::cta.b64 p2, [%3], %5;\n"
-      "mbarrier.test_wait.parity.shared::cta.b64 p3, [%4], %5;\n"
-      "and.pred p0, p0, p1;\n"
-      "and.pred p2, p2, p3;\n"
-      "and.pred p0, p0, p2;\n"
-      "selp.u32 %0, 1, 0, p0;\n"
-      "}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bars)), "r"(smem_u32(bars + 1)), "r"(smem_u32(bars + 2)), "r"(smem_u32(bars + 3)),
-        "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -64,11 +64,12 @@ def _desc(**kw):
     (dict(page_size=32), -2), (dict(num_q_heads=6, num_kv_heads=4), -1), (dict(batch=0), -1),
     (dict(dtype=7), -2), (dict(kernel=9), -1), (dict(kernel=2, dtype=0), -2),
     (dict(num_splits=-1), -1), (dict(sm_scale=float("nan")), -1),
-    # FP8 cache: E4M3 only, as a cache type only, positive finite scales, not on tensor cores
+    # FP8 cache: E4M3 only, as a cache type only, positive finite scales, and on
+    # tensor cores only with a 16-bit act dtype
     (dict(dtype=3), -2), (dict(cache_dtype=5), -2), (dict(cache_dtype=1), -2),
     (dict(cache_dtype=3, k_scale=0.0), -1), (dict(cache_dtype=3, v_scale=-1.0), -1),
     (dict(cache_dtype=3, k_scale=float("nan")), -1), (dict(cache_dtype=3, v_scale=float("inf")), -1),
-    (dict(cache_dtype=3, kernel=2), -2),
+    (dict(cache_dtype=3, kernel=2, dtype=0), -2),
 ])
 def test_attn_rejects_bad_descriptors(lib, kw, code):
     d = _desc(**kw)
@@ -235,3 +236,4 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
 def test_debug_set_wait_refuses_bad_stall(lib):
     assert lib.mt_debug_set_wait(0, 2) == -1
     assert lib.mt_debug_set_wait(0, 0) == 0
+

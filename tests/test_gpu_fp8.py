@@ -45,7 +45,7 @@ def _step(w, kc, vc, k_scale, v_scale, num_splits=0, kernel="auto"):
     step.d["k_cache"] = torch.from_numpy(kc).view(torch.float8_e4m3fn).cuda()
     step.d["v_cache"] = torch.from_numpy(vc).view(torch.float8_e4m3fn).cuda()
     step.k_scale, step.v_scale = float(k_scale), float(v_scale)
-    # an FP8 cache runs the CUDA-core kernel, whose workspace differs from the tensor-core one
+    # the workspace for the kernel that runs (its size depends on the kernel)
     desc = mt.make_desc(step.d["q"], step.d["k_cache"], step.d["block_tables"], num_splits, kernel,
                         k_scale=max(float(k_scale), 1.0), v_scale=max(float(v_scale), 1.0))
     if mt.attn_workspace_size(desc) > 0:   # (0 for a descriptor the library refuses)
@@ -67,11 +67,14 @@ SCALES = [(0.0113, 0.0127), (0.004, 0.02)]
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 @pytest.mark.parametrize("case", [c[0] for c in CASES])
 @pytest.mark.parametrize("splits", [0, 3])
-def test_fp8_attention_and_scatter(dtype, case, splits):
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+def test_fp8_attention_and_scatter(dtype, case, splits, kernel):
+    if dtype == "f32" and kernel == "tc":
+        pytest.skip("the tensor-core kernel takes fp16/bf16 act dtypes")
     spec = workloads.custom(case, dtype=dtype, **dict(CASES)[case])
     for seed, (ks, vs) in enumerate(SCALES):
         w, kc, vc = _fp8_workload(spec, seed, ks, vs)
-        step = _step(w, kc, vc, ks, vs, num_splits=splits)
+        step = _step(w, kc, vc, ks, vs, num_splits=splits, kernel=kernel)
         step.attn()
         assert step.status()[0] == 0
         q_rot, kc2, vc2 = _oracle_scatter(w, kc, vc, ks, vs)
@@ -144,14 +147,44 @@ def test_fp8_two_call_commit_moves_codes():
     assert np.array_equal(to_host(step.d["v_cache"]), vo)
 
 
-def test_fp8_cache_is_refused_on_the_tensor_core_kernel():
-    spec = workloads.custom("fp8tc", dtype="bf16", **dict(CASES)["fanout_gqa"])
+def test_fp8_refusals():
+    # fp32 act values have no tensor-core kernel, FP8 cache or not
+    spec = workloads.custom("fp8tc32", dtype="f32", **dict(CASES)["fanout_gqa"])
     w, kc, vc = _fp8_workload(spec, 0, 0.0113, 0.0127)
-    step = _step(w, kc, vc, 0.0113, 0.0127, kernel="tc")
+    step = _step(w, kc, vc, 0.0113, 0.0127)
+    step.kernel = "tc"
     with pytest.raises(mt.MedusaTreeError) as e:
         step.attn()
     assert e.value.status == -2
+    # a scale that is not positive
+    spec = workloads.custom("fp8tc", dtype="bf16", **dict(CASES)["fanout_gqa"])
+    w, kc, vc = _fp8_workload(spec, 0, 0.0113, 0.0127)
     step = _step(w, kc, vc, 0.0, 0.0127)
     with pytest.raises(mt.MedusaTreeError) as e:
         step.attn()
     assert e.value.status == -1
+
+
+@pytest.mark.parametrize("name", ["serve_b16_gqa_bf16", "verify_b64_fp16"])
+def test_fp8_tensor_core_full_size(name):
+    # the named workloads' caches as E4M3 codes (amax-style scales), every
+    # output against the oracle's reading of the same codes
+    w = workloads.generate(name, seed=2, backend="torch", device="cuda")
+    w_np = workloads.to_numpy(w)
+    ks, vs = 0.0113, 0.0127
+    # the cache contents are inputs: torch's own E4M3 cast of value / scale,
+    # clamped to +-448 (its cast does not saturate); the oracle alone gives
+    # the expected codes of the tree slots and the outputs
+    codes = lambda c, sc: ((c.float() / sc).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+                           .view(torch.uint8).cpu().numpy())
+    kc, vc = codes(w["k_cache"], ks), codes(w["v_cache"], vs)
+    step = _step(w, kc, vc, ks, vs, kernel="tc")
+    step.attn()
+    assert step.status()[0] == 0
+    q_rot, kc2, vc2 = _oracle_scatter(w_np, kc, vc, ks, vs)
+    assert np.array_equal(to_host(step.d["k_cache"]), kc2)
+    assert np.array_equal(to_host(step.d["v_cache"]), vc2)
+    want = oracle.tree_attn_e4m3(w_np, kc2, vc2, ks, vs, q_rot=q_rot)
+    got = step.out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    assert np.max(np.abs(got - want)) <= TOL[w_np["dtype"]]
