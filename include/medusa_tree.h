@@ -222,9 +222,10 @@ int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
                           cudaStream_t stream);
 
 /* ---- Typical acceptance ---------------------------------------------------
- * The "typical acceptance scheme" that lmdeploy PR 1231 ("[WIP] support
- * Medusa") names beside tree attention; the pages do not define it, and the
- * rule taken is the Medusa paper's (Cai et al. 2024, typical acceptance).
+ * The "typical acceptance scheme" that the opening comment of vLLM issue 1171
+ * (gesanqiu: tree attention and typical acceptance are what most inference
+ * frameworks lack) names beside tree attention; the pages do not define it, and
+ * the rule taken is the Medusa paper's (Cai et al. 2024, typical acceptance).
  * Per sequence b, with x the logits row of a node and tau = temperature:
  *   q_v = exp(x_v / tau) / sum_u exp(x_u / tau), H = -sum_v q_v ln q_v;
  *   node i > 0 passes when q[tree_tokens[b][i]] > min(epsilon, delta * exp(-H))

@@ -12,9 +12,9 @@
 // writes accept_len, the padded root-to-end path and next_token, and, in the
 // fused form, commits the sequence's K/V (commit_seq.cuh) right away.
 //
-// Typical acceptance (the scheme lmdeploy PR 1231 names beside tree attention;
-// the rule of the Medusa paper) has the same shape: each row's CTA streams its
-// logits once for the argmax and the tempered distribution's statistics, and
+// Typical acceptance (the scheme named beside tree attention in the opening
+// comment of vLLM issue 1171; the rule of the Medusa paper) has the same shape:
+// each row's CTA streams its logits once for the argmax and the tempered distribution's statistics, and
 // node i > 0 passes when its token's probability under its parent's row is
 // above min(epsilon, delta * exp(-entropy)).
 #include "commit_seq.cuh"

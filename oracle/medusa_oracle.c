@@ -22,9 +22,10 @@
  *    answer by rakib-hasan: a position-offset tensor makes RoPE rotate each
  *    Medusa token at its own position (prefix length + tree depth here).
  *  - lmdeploy PR 1231 "[WIP] support Medusa": greedy acceptance at LM-head
- *    temperature 0 (`evaluate_posterior`), verified with a 64-choice tree; a
- *    "typical acceptance scheme" is named there but not defined (the reading
- *    taken is stated at or_accept_typical).
+ *    temperature 0 (`evaluate_posterior`), verified with a 64-choice tree.
+ *  - vLLM issue 1171, opening comment (gesanqiu): a "typical acceptance
+ *    scheme" is named beside tree attention but not defined (the reading taken
+ *    is stated at or_accept_typical).
  *
  * Readings the pages leave open (the node-0 root at position prefix_len,
  * self-visibility, NeoX half-split RoPE pairing, 1/sqrt(D) scale, lowest index
@@ -544,7 +545,7 @@ int or_accept_greedy(int dt, int B, int T, int V, int max_depth, const int32_t* 
 
 /* Typical acceptance.  The pages name a "typical acceptance scheme" beside
  * tree attention as the part of Medusa that inference frameworks lack
- * (lmdeploy PR 1231, comment on adopting Medusa heads) but never define it.
+ * (vLLM issue 1171, opening comment by gesanqiu) but never define it.
  * Reading taken, from the Medusa paper's typical-acceptance rule (Cai et al.,
  * "Medusa: Simple LLM Inference Acceleration Framework with Multiple Decoding
  * Heads", 2024), restated: a tree node i > 0 passes when the target model's
