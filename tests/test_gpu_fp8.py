@@ -86,6 +86,37 @@ def test_fp8_attention_and_scatter(dtype, case, splits, kernel):
         assert err <= TOL[dtype], f"max abs error {err}"
 
 
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("kernel", ["simt", "tc"])
+def test_fp8_subnormal_and_every_code_read_exactly(dtype, kernel):
+    # Prefix keys drawn from the 14 subnormal codes only, under a K scale that
+    # makes the scores depend on them entirely (a reading that flushed them to
+    # zero would turn the prefix attention uniform); prefix values drawn from
+    # every finite code.  Slots that hold NaN codes (outside the sequences)
+    # keep them.  The tree's own K/V codes come from the prep kernel as usual.
+    spec = workloads.custom("f8codes", dtype=dtype, **dict(CASES)["fanout_gqa"])
+    w, kc, vc = _fp8_workload(spec, 3, 0.0113, 0.0127)
+    rng = np.random.default_rng(7)
+    sub = np.array([s | m for s in (0x00, 0x80) for m in range(1, 8)], dtype=np.uint8)
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    kc = np.where((kc & 0x7F) == 0x7F, kc, rng.choice(sub, kc.shape)).astype(np.uint8)
+    vc = np.where((vc & 0x7F) == 0x7F, vc, rng.choice(finite, vc.shape)).astype(np.uint8)
+    ks, vs = 300.0, 1.0 / 448.0
+    step = _step(w, kc, vc, ks, vs, kernel=kernel)
+    step.attn()
+    assert step.status()[0] == 0
+    q_rot, kc2, vc2 = _oracle_scatter(w, kc, vc, ks, vs)
+    assert np.array_equal(to_host(step.d["k_cache"]), kc2)
+    want = oracle.tree_attn_e4m3(w, kc2, vc2, ks, vs, q_rot=q_rot)
+    got = step.out.float().cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - want)) <= TOL[dtype]
+    # the prefix scores matter: the same call with the subnormal keys zeroed
+    # gives outputs far from these
+    kz = np.where(np.isin(kc, sub), np.uint8(0), kc).astype(np.uint8)
+    flat = oracle.tree_attn_e4m3(w, *_oracle_scatter(w, kz, vc, ks, vs)[1:], ks, vs, q_rot=q_rot)
+    assert np.max(np.abs(flat - want)) > 20 * TOL[dtype]
+
+
 def test_fp8_tight_scale_saturates_tree_keys():
     spec = workloads.custom("sat", dtype="bf16", **dict(CASES)["fanout_gqa"])
     w, kc, vc = _fp8_workload(spec, 0, 0.004, 0.02)
