@@ -12,6 +12,8 @@
 // [B][T][Hq][D] workspace array read by the attention kernels.
 #include <cuda_fp8.h>
 
+#include <atomic>
+
 #include "kernels.cuh"
 
 namespace mt {
@@ -19,6 +21,7 @@ namespace mt {
 namespace {
 
 constexpr int kPrepThreads = 256;
+constexpr int kMaxDevices = 64;
 
 // 8 consecutive act-dtype elements as one aligned vector.
 template <typename T> struct Vec8 {
@@ -346,26 +349,46 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
   }
 }
 
+template <typename T>
+cudaError_t launch_t(const PrepParams& a, cudaStream_t stream) {
+  const long long nrows = (long long)a.B * a.T * ((long long)a.Hq + a.Hkv);
+  const long long rows_per_block = (long long)(kPrepThreads / 32) * (32 / (a.D / 16));
+  size_t smem = sizeof(int) * (size_t)(2 * a.B + 1);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  // One resident wave: the rotation loop strides over the grid, so blocks
+  // beyond what the SMs hold at once would only form a second, short wave.
+  // The number resident per SM is looked up once per device.
+  static std::atomic<int> resident[kMaxDevices];
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  int per_sm = dev >= 0 && dev < kMaxDevices ? resident[dev].load(std::memory_order_relaxed) : 0;
+  if (per_sm <= 0) {
+    // without the dynamic part (block 0's per-sequence arrays, a few KB up to
+    // batches in the thousands): a batch so large that it lowers residency
+    // only gets a short extra wave, which is correct, as no block waits for
+    // another
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prep_kernel<T>, kPrepThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    if (dev >= 0 && dev < kMaxDevices) resident[dev].store(per_sm, std::memory_order_relaxed);
+  }
+  long long blocks = (nrows + rows_per_block - 1) / rows_per_block + 1;  // + block 0 (the schedule)
+  const long long wave = (long long)per_sm * sms;
+  if (blocks > wave) blocks = wave;
+  if (blocks < 2) blocks = 2;
+  return launch_pdl(prep_kernel<T>, dim3((unsigned)blocks), dim3(kPrepThreads), smem, stream, a);
+}
+
 }  // namespace
 
 cudaError_t launch_prep(const PrepParams& a, int dtype, cudaStream_t stream) {
-  const long long nrows = (long long)a.B * a.T * ((long long)a.Hq + a.Hkv);
-  const long long rows_per_block = (long long)(kPrepThreads / 32) * (32 / (a.D / 16));
-  int sms = 148;
-  int dev = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess)
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long blocks = (nrows + rows_per_block - 1) / rows_per_block;
-  if (blocks > 8LL * sms) blocks = 8LL * sms;
-  if (blocks < 1) blocks = 1;
-  blocks += 1;  // block 0 builds the schedule
-  size_t smem = sizeof(int) * (size_t)(2 * a.B + 1);
-  if (smem > 48 * 1024) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)blocks);
   switch (dtype) {
-    case 0: return launch_pdl(prep_kernel<float>, grid, dim3(kPrepThreads), smem, stream, a);
-    case 1: return launch_pdl(prep_kernel<__half>, grid, dim3(kPrepThreads), smem, stream, a);
-    default: return launch_pdl(prep_kernel<__nv_bfloat16>, grid, dim3(kPrepThreads), smem, stream, a);
+    case 0: return launch_t<float>(a, stream);
+    case 1: return launch_t<__half>(a, stream);
+    default: return launch_t<__nv_bfloat16>(a, stream);
   }
 }
 
