@@ -17,6 +17,8 @@
 // each row's CTA streams its logits once for the argmax and the tempered distribution's statistics, and
 // node i > 0 passes when its token's probability under its parent's row is
 // above min(epsilon, delta * exp(-entropy)).
+#include <atomic>
+
 #include "commit_seq.cuh"
 
 namespace mt {
@@ -239,15 +241,27 @@ __device__ void finish_row(const AcceptParams& a, const CommitParams& c, int row
   }
 }
 
-// Per-node argmax, one CTA per row, for rows of 16-byte vectors.  Each thread
-// takes the vectors tid, tid + kRowThreads, ... in increasing index order,
-// kBatch of them per round with all their loads issued before any is used
-// (streaming loads: the logits are read once), keeping (max, first index): a
-// vector's packed maximum is compared first and the vector is searched only
-// when it beats the running maximum.  Warps, then the block, merge the
-// threads' results in the same order.
+// Per-node argmax for rows of 16-byte vectors, one CTA per row, or, when the
+// rows are few, a.nsplit CTAs per row, each taking one contiguous slice of the
+// row's vectors.  Each thread takes its slice's vectors tid, tid +
+// kRowThreads, ... in increasing index order, kBatch of them per round with
+// all their loads issued before any is used (streaming loads: the logits are
+// read once), keeping (max, first index): a vector's packed maximum is
+// compared first and the vector is searched only when it beats the running
+// maximum.  Warps, then the block, merge the threads' results in the same
+// order.  The slices of a split row meet in a 64-bit key (below); the last
+// slice to arrive continues as the row's CTA.
 constexpr int kRowThreads = 128;
 constexpr int kBatch = 8;
+
+// (value, index) as a key whose unsigned order is the argmax order: a larger
+// value first, then a lower index; -0 counts as +0.  No NaN (precondition).
+__device__ __forceinline__ unsigned long long argmax_key(float v, int ix) {
+  if (v == 0.f) v = 0.f;
+  const uint32_t bits = __float_as_uint(v);
+  const uint32_t ord = (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (0xffffffffu - (uint32_t)ix);
+}
 
 template <typename T, bool kCommit>
 __global__ void __launch_bounds__(kRowThreads, 8) argmax_rows_kernel(AcceptParams a, CommitParams c, int stage_vecs) {
@@ -256,26 +270,29 @@ __global__ void __launch_bounds__(kRowThreads, 8) argmax_rows_kernel(AcceptParam
   __shared__ float s_v[kRowThreads / 32];
   __shared__ int s_i[kRowThreads / 32];
   __shared__ FinishSmem sm;
+  __shared__ int s_slice_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x;
+  const int row = blockIdx.x / a.nsplit, slice = blockIdx.x % a.nsplit;
   pdl_wait();
   SeqPrefetch pf;
   pf.load(a, c, row / a.T, kCommit);
   const int nvec = a.V / EPV;
+  const int per = (nvec + a.nsplit - 1) / a.nsplit;
+  const int vbeg = slice * per, vend = min(nvec, vbeg + per);
   const uint4* lg = reinterpret_cast<const uint4*>(static_cast<const T*>(a.logits) + (size_t)row * a.V);
   float best = -INFINITY;
   int bidx = 0x7fffffff;
-  for (int v0 = tid; v0 < nvec; v0 += kRowThreads * kBatch) {
+  for (int v0 = vbeg + tid; v0 < vend; v0 += kRowThreads * kBatch) {
     uint4 raw[kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int v = v0 + j * kRowThreads;
-      if (v < nvec) raw[j] = __ldcs(lg + v);
+      if (v < vend) raw[j] = __ldcs(lg + v);
     }
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int v = v0 + j * kRowThreads;
-      if (v < nvec) {
+      if (v < vend) {
         const float m = Max8<T>::of(raw[j]);
         if (m > best || bidx == 0x7fffffff) {
           T tmp[EPV];
@@ -298,6 +315,23 @@ __global__ void __launch_bounds__(kRowThreads, 8) argmax_rows_kernel(AcceptParam
   float v = lane < kRowThreads / 32 ? s_v[lane] : -INFINITY;
   int ix = lane < kRowThreads / 32 ? s_i[lane] : 0x7fffffff;
   warp_best(v, ix);  // every warp merges; thread 0's result is used
+  if (a.nsplit > 1) {
+    // fold this slice into the row's key and count it; the row's last slice
+    // takes the key (leaving it and the counter at zero) and goes on
+    if (tid == 0) {
+      atomicMax(&a.row_keys[row], argmax_key(v, ix));
+      __threadfence();  // the key is updated before the arrival is counted
+      const bool last = atomicAdd(&a.row_counters[row], 1u) == (unsigned)(a.nsplit - 1);
+      if (last) {
+        __threadfence();  // every slice's key update is visible past this point
+        ix = (int)(0xffffffffu - (uint32_t)atomicExch(&a.row_keys[row], 0ull));
+        a.row_counters[row] = 0;
+      }
+      s_slice_last = last;
+    }
+    __syncthreads();
+    if (!s_slice_last) return;
+  }
   finish_row<kCommit>(a, c, row, ix, sm, stage, stage_vecs);
 }
 
@@ -534,14 +568,37 @@ cudaError_t launch_typical_t(const AcceptParams& a, const TypicalParams& t, cuda
 // bf16 heads of 128 fit in one pass).
 constexpr int kStageCap = 20 * 1024;
 
+// CTAs per row for the vector kernel: one, unless the rows are fewer than
+// about four CTAs per SM; then enough slices to reach that, each of at least
+// 256 vectors (two rounds of loads per thread).
+inline int row_splits(int nrows, int nvec) {
+  static std::atomic<int> sms_cached{0};
+  int sms = sms_cached.load(std::memory_order_relaxed);
+  if (sms <= 0) {
+    int dev = 0;
+    sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    sms_cached.store(sms, std::memory_order_relaxed);
+  }
+  const long long target = 4LL * sms;
+  if (nrows >= target) return 1;
+  const int want = (int)((target + nrows - 1) / nrows);
+  const int most = nvec / 256;
+  return most < 2 ? 1 : (want < most ? want : most);
+}
+
 template <typename T, bool kCommit>
 cudaError_t launch_t(const AcceptParams& a, const CommitParams& c, cudaStream_t stream) {
   const int nrows = a.B * a.T;
   const int sv = kCommit ? commit_stage_vecs(c, kStageCap) : 0;
   const size_t smem = (size_t)sv * 16;
+  AcceptParams p = a;
+  p.nsplit = 1;
   if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0)
-    return launch_pdl(argmax_scalar_kernel<T, kCommit>, dim3(nrows), dim3(kThreads), smem, stream, a, c, sv);
-  return launch_pdl(argmax_rows_kernel<T, kCommit>, dim3(nrows), dim3(kRowThreads), smem, stream, a, c, sv);
+    return launch_pdl(argmax_scalar_kernel<T, kCommit>, dim3(nrows), dim3(kThreads), smem, stream, p, c, sv);
+  p.nsplit = row_splits(nrows, (int)(a.V / (16 / sizeof(T))));
+  return launch_pdl(argmax_rows_kernel<T, kCommit>, dim3((unsigned)((long long)nrows * p.nsplit)),
+                    dim3(kRowThreads), smem, stream, p, c, sv);
 }
 
 template <bool kCommit>

@@ -294,9 +294,11 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
 }
 
 // Acceptance workspace: status word, arrival counters [B], then (typical
-// acceptance) each row's argmax [B*T] int32 and statistics [B*T] float4.
+// acceptance) each row's argmax [B*T] int32 and statistics [B*T] float4, then
+// (rows split over several CTAs) each row's key [B*T] uint64 and slice
+// counter [B*T] uint32.
 struct AcceptWs {
-  size_t counters, argmax, stats, total;
+  size_t counters, argmax, stats, row_keys, row_counters, total;
 };
 
 AcceptWs accept_ws(int batch, int tree_size) {
@@ -305,8 +307,17 @@ AcceptWs accept_ws(int batch, int tree_size) {
   w.counters = kAlign;
   w.argmax = align_up(w.counters + sizeof(unsigned) * (size_t)batch);
   w.stats = align_up(w.argmax + sizeof(int) * rows);
-  w.total = align_up(w.stats + sizeof(float4) * rows);
+  w.row_keys = align_up(w.stats + sizeof(float4) * rows);
+  w.row_counters = align_up(w.row_keys + sizeof(unsigned long long) * rows);
+  w.total = align_up(w.row_counters + sizeof(unsigned) * rows);
   return w;
+}
+
+// The split-row scratch of an acceptance workspace.
+void set_row_scratch(AcceptParams& a, char* ws, int batch, int tree_size) {
+  const AcceptWs w = accept_ws(batch, tree_size);
+  a.row_keys = reinterpret_cast<unsigned long long*>(ws + w.row_keys);
+  a.row_counters = reinterpret_cast<unsigned*>(ws + w.row_counters);
 }
 
 size_t mt_tree_accept_workspace_size(int batch, int tree_size) {
@@ -338,6 +349,7 @@ int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
   a.argmax_out = argmax_out; a.accept_len = accept_len; a.accept_path = accept_path;
   a.next_token = next_token;
   a.status = reinterpret_cast<int*>(ws);
+  set_row_scratch(a, ws, batch, tree_size);
   a.counters = reinterpret_cast<unsigned*>(ws + accept_ws(batch, tree_size).counters);
   return cuda_status(launch_accept(a, logits_dtype, stream));
 }
@@ -371,6 +383,7 @@ int mt_tree_accept_typical(int batch, int tree_size, int vocab, int max_depth,
   a.argmax_out = reinterpret_cast<int*>(ws + w.argmax);
   a.accept_len = accept_len; a.accept_path = accept_path; a.next_token = next_token;
   a.status = reinterpret_cast<int*>(ws);
+  set_row_scratch(a, ws, batch, tree_size);
   a.counters = reinterpret_cast<unsigned*>(ws + w.counters);
   TypicalParams t{};
   t.k = k; t.epsilon = epsilon; t.delta = delta;
@@ -431,6 +444,7 @@ int mt_tree_accept_commit(const mt_attn_desc* d, int vocab, int max_depth, mt_dt
   a.argmax_out = argmax_out; a.accept_len = accept_len; a.accept_path = accept_path;
   a.next_token = next_token;
   a.status = reinterpret_cast<int*>(ws);
+  set_row_scratch(a, ws, batch, tree_size);
   a.counters = reinterpret_cast<unsigned*>(ws + accept_ws(batch, tree_size).counters);
   CommitParams c{};
   c.B = batch; c.T = tree_size; c.Hkv = d->num_kv_heads; c.D = d->head_dim;

@@ -80,6 +80,13 @@ struct AcceptParams {
   int* next_token;
   int* status;
   unsigned int* counters;  // [B], left at zero
+  // A row split over nsplit CTAs (few rows: more CTAs than rows keep the GPU
+  // busy): the slices fold their best (value, lowest index) into row_keys and
+  // count themselves in row_counters; the last slice continues as the row's
+  // CTA.  Both [B*T], left at zero.
+  unsigned long long* row_keys;
+  unsigned int* row_counters;
+  int nsplit;
 };
 
 // Typical acceptance's extra arguments (accept.cu).

@@ -16,7 +16,7 @@ from gpu_helpers import Step, to_dev, to_host
 pytestmark = pytest.mark.gpu
 
 
-def _accept_dev(tokens, logits, dt, parents, md):
+def _accept_dev(tokens, logits, dt, parents, md, ws=None):
     dev = "cuda"
     B, T = tokens.shape
     t_tok = torch.from_numpy(np.ascontiguousarray(tokens, np.int32)).to(dev)
@@ -26,7 +26,8 @@ def _accept_dev(tokens, logits, dt, parents, md):
     alen = torch.full((B,), -7, dtype=torch.int32, device=dev)
     path = torch.full((B, md + 1), -7, dtype=torch.int32, device=dev)
     nxt = torch.full((B,), -7, dtype=torch.int32, device=dev)
-    ws = mt.alloc_accept_workspace(B, T, dev)
+    if ws is None:
+        ws = mt.alloc_accept_workspace(B, T, dev)
     mt.tree_accept_greedy(t_tok, t_lg, t_par, alen, path, argmax_out=am, next_token=nxt, workspace=ws)
     st = mt.read_status(ws)
     return st, am.cpu().numpy(), alen.cpu().numpy(), path.cpu().numpy(), nxt.cpu().numpy(), ws
@@ -54,6 +55,37 @@ def test_accept_random_small_vocab(dt, V):
         assert np.array_equal(alen, o_len)
         assert np.array_equal(path, o_path)
         assert np.array_equal(nxt, o_next)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("V", [4096, 6000, 32000])
+def test_accept_split_rows_with_ties_across_slices(dt, V):
+    # Few rows and long vocabularies: each row is split over several CTAs
+    # whose (value, lowest index) results meet in a per-row key.  Values from
+    # {-2 .. 2} with signed zeros put equal maxima in many slices; the lowest
+    # index must still win, and a second call on the same workspace (keys and
+    # counters left at zero) must give the same answer.
+    rng = np.random.default_rng(V)
+    for B, T in ((1, 1), (1, 9), (3, 5)):
+        parents = np.zeros((B, T), np.int32)
+        for b in range(B):
+            parents[b] = [-1] + [int(rng.integers(i)) for i in range(1, T)]
+        md = int(np.stack([workloads.depths_of(p) for p in parents]).max())
+        logits = rng.integers(-2, 3, (B, T, V)).astype(np.float32)
+        logits[logits == 0] *= rng.choice([-1.0, 1.0], size=int((logits == 0).sum()))
+        # some rows whose maximum sits only near the end of the row
+        logits[:, 0, :] = np.minimum(logits[:, 0, :], 1.0)
+        logits[:, 0, V - 3] = 2.0
+        tokens = rng.integers(0, V, (B, T)).astype(np.int32)
+        lg = oracle.round_to_act(logits, dt)
+        o = oracle.accept_greedy(tokens, lg, dt, parents, md)
+        ws = None
+        for _ in range(2):
+            st, am, alen, path, nxt, ws = _accept_dev(tokens, lg, dt, parents, md, ws)
+            assert st == 0
+            for got, want in zip((am, alen, path, nxt), o):
+                assert np.array_equal(got, want)
+        assert (o[0][:, 0] == V - 3).all()
 
 
 @pytest.mark.parametrize("name", ["tiny_tree_fp32", "llama7b_b1_fp16", "serve_b16_gqa_bf16",
