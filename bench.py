@@ -379,6 +379,64 @@ def run_ours(args, rank, world, local_rank):
         breakdown["tree_accept_typical_ms"] = float(np.mean([a.elapsed_time(b) for a, b in evt]))
         breakdown["typical"] = typical
 
+    # The per-call times above bracket eager calls, so for small workloads they
+    # include the GPU idling while the host runs the binding's checks.  Each
+    # call is also replayed alone as a CUDA graph (L2 flushed and tables
+    # restored before each replay, outside the events); with graphs on, these
+    # are the breakdown's times.
+    if not args.no_graph:
+        def attn_call():
+            mt.tree_attn_paged(w["q"], w["k_cache"], w["v_cache"], w["block_tables"], w["seq_lens"],
+                               w["tree_parents"], w["tree_depths"], out, k_new=w["k_new"], v_new=w["v_new"],
+                               rope=rope, workspace=ws, num_splits=args.splits, kernel=args.kernel,
+                               k_scale=k_scale, v_scale=v_scale)
+
+        calls = {"tree_attn_paged_ms": attn_call}
+        if has_accept:
+            calls["tree_accept_greedy_ms"] = lambda: mt.tree_accept_greedy(
+                w["tree_tokens"], w["logits"], w["tree_parents"], alen, path, argmax_out=am, next_token=nxt,
+                workspace=aws)
+            calls["kv_commit_ms"] = lambda: mt.kv_commit(path, alen, w["k_cache"], w["v_cache"],
+                                                         w["block_tables"], w["seq_lens"], rel, tree_size=T,
+                                                         status_ws=ws)
+            calls["tree_accept_commit_ms"] = lambda: mt.tree_accept_commit(
+                w["tree_tokens"], w["logits"], w["tree_parents"], alen, path, w["k_cache"], w["v_cache"],
+                w["block_tables"], w["seq_lens"], rel, argmax_out=am, next_token=nxt, workspace=aws)
+            if evt:
+                calls["tree_accept_typical_ms"] = lambda: mt.tree_accept_typical(
+                    w["tree_tokens"], w["logits"], w["tree_parents"], alen, path, node_accept=node_ok,
+                    next_token=nxt, workspace=aws, **typical)
+        cs_g = torch.cuda.Stream(device=dev)
+        for key, fn in calls.items():
+            restore()
+            cs_g.wait_stream(stream)
+            with torch.cuda.stream(cs_g):
+                fn()                         # warm the capture stream
+                cs_g.synchronize()
+                restore()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cs_g):
+                    fn()
+            stream.wait_stream(cs_g)
+            torch.cuda.synchronize()
+            pairs = []
+            for k in range(K):
+                restore()
+                flush.fill_(k & 0xFF)
+                e_a, e_b = mk(), mk()
+                e_a.record(stream)
+                g.replay()
+                e_b.record(stream)
+                pairs.append((e_a, e_b))
+            torch.cuda.synchronize()
+            breakdown[key] = float(np.mean([x.elapsed_time(y) for x, y in pairs]))
+            del g
+        breakdown["note"] = ("each call replayed alone as a CUDA graph, L2 flushed and tables restored before "
+                             "each replay (outside the events); the step uses " + {
+                                 "fused": "tree_accept_commit", "separate": "tree_accept_greedy + kv_commit",
+                                 "typical": "tree_accept_typical + kv_commit"}[args.accept])
+    restore()
+
     # (2) the timed steps: the whole step replayed as one CUDA graph (or
     # launched kernel by kernel with --no-graph)
     graph = None

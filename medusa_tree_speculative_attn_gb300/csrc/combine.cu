@@ -125,7 +125,24 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(Attn
       for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
       const int r = in.row0 + lane;
       const bool row_ok = r < PR && rg * RG + r < a.rows;
-      if (row_ok) {
+      if (row_ok && !in.all && s.splits == 0) {
+        // a sparse schedule (fewer cost units than CTAs): most CTAs between the
+        // segment's first and last owners hold nothing, so walk the segment's
+        // tiles and take each distinct owner's partial slot once
+        const long long t0 = (long long)s.tile_pfx[b] * HR + (long long)seg_in_b * in.nt;
+        int prev = -1;
+        for (int t = 0; t < in.nt; ++t) {
+          const int cta = sched_cta_of(sched_tile_cost(s, t0 + t, in.seg), W, s.G);
+          if (cta == prev) continue;
+          prev = cta;
+          const size_t slot = (size_t)in.seg + cta;
+          float4 v1[PER];
+          const float2 ml1 = a.part_ml[slot * PR + r];
+#pragma unroll
+          for (int e = 0; e < PER; ++e) v1[e] = a.part_o[(slot * C4 + warp + kWarps * e) * PR + r];
+          merge<PER>(M, lsum, acc, ml1, v1);
+        }
+      } else if (row_ok) {
         for (int k = 0; k < in.count; k += kRound) {
           float2 ml[kRound];
           float4 v[kRound][PER];
