@@ -371,6 +371,14 @@ __global__ void __launch_bounds__(kThreads) argmax_scalar_kernel(AcceptParams a,
 // in bits is H = log2 Z - S / Z (H ln 2 in nats, and exp(-H ln 2) = 2^-H).
 // Each thread keeps a running (m, Z, S), moved to a larger m by scaling
 // (Z, S) -> (c Z, c (S + (m_old - m) Z)), c = 2^(m_old - m).
+// 2^x on the MUFU pipe (results below 2^-126 flush to zero: such terms add
+// nothing measurable to a row's Z and S).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 struct RowStats {
   float m = -INFINITY, z = 0.f, s = 0.f;
   __device__ __forceinline__ void rebase(float nm) {  // nm >= m
@@ -489,45 +497,73 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
         else xs[j] = Act<T>::to_f(base[v]);
       }
     }
-    // pass 1: argmax and the round's largest y
-    float bm = -INFINITY;
+    if constexpr (kVec) {
+      // pass 1, per vector: its packed maximum decides the argmax (searched
+      // only when it beats the running one, as in the greedy kernel) and the
+      // round's largest y (k > 0, so max of x * k is k * max of x, exactly)
+      float bm = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int v = v0 + j * kRowThreads;
-      if (v < nvec) {
-        float x[EPV];
-        if constexpr (kVec) {
-          T tmp[EPV];
-          memcpy(tmp, &raw[j], 16);
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = v0 + j * kRowThreads;
+        if (v < nvec) {
+          const float m8 = Max8<T>::of(raw[j]);
+          if (m8 > best || bidx == 0x7fffffff) {
+            T tmp[EPV];
+            memcpy(tmp, &raw[j], 16);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) x[e] = Act<T>::to_f(tmp[e]);
-        } else {
-          x[0] = xs[j];
-        }
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          if (x[e] > best || bidx == 0x7fffffff) {  // indices rise within a thread: the first maximum stays
-            best = x[e];
-            bidx = v * EPV + e;
+            for (int e = EPV - 1; e >= 0; --e)
+              if (Act<T>::to_f(tmp[e]) == m8) bidx = v * EPV + e;
+            best = m8;
           }
-          bm = fmaxf(bm, x[e] * t.k);
+          bm = fmaxf(bm, m8);
         }
       }
-    }
-    // pass 2: the round's terms, under the running maximum
-    if (bm > st.m) st.rebase(bm);
+      // pass 2: the round's terms under the running maximum, d = y - m in one
+      // rounding, two accumulator pairs (a term that underflows adds 0 to both)
+      bm *= t.k;
+      if (bm > st.m) st.rebase(bm);
+      const float neg_m = -st.m;
+      float z0 = 0.f, z1 = 0.f, s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < kBatch; ++j) {
-      const int v = v0 + j * kRowThreads;
-      if (v < nvec) {
-        if constexpr (kVec) {
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = v0 + j * kRowThreads;
+        if (v < nvec) {
           T tmp[EPV];
           memcpy(tmp, &raw[j], 16);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) st.add(Act<T>::to_f(tmp[e]) * t.k);
-        } else {
-          st.add(xs[j] * t.k);
+          for (int e = 0; e < EPV; e += 2) {
+            const float d0 = fmaf(Act<T>::to_f(tmp[e]), t.k, neg_m);
+            const float d1 = fmaf(Act<T>::to_f(tmp[e + 1]), t.k, neg_m);
+            const float e0 = fast_exp2(d0), e1 = fast_exp2(d1);
+            z0 += e0;
+            z1 += e1;
+            s0 = fmaf(e0, d0, s0);
+            s1 = fmaf(e1, d1, s1);
+          }
         }
+      }
+      st.z += z0 + z1;
+      st.s += s0 + s1;
+    } else {
+      // pass 1: argmax and the round's largest y
+      float bm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = v0 + j * kRowThreads;
+        if (v < nvec) {
+          if (xs[j] > best || bidx == 0x7fffffff) {  // indices rise within a thread: the first maximum stays
+            best = xs[j];
+            bidx = v;
+          }
+          bm = fmaxf(bm, xs[j] * t.k);
+        }
+      }
+      // pass 2: the round's terms, under the running maximum
+      if (bm > st.m) st.rebase(bm);
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int v = v0 + j * kRowThreads;
+        if (v < nvec) st.add(xs[j] * t.k);
       }
     }
   }
