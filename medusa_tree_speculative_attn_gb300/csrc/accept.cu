@@ -476,7 +476,8 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
   __shared__ int typ_ok[kMaxTree];
   __shared__ FinishSmem sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x;
+  __shared__ int s_slice_last;
+  const int row = blockIdx.x / a.nsplit, slice = blockIdx.x % a.nsplit;
   pdl_wait();
   SeqPrefetch pf;
   pf.load(a, CommitParams{}, row / a.T, false);
@@ -485,14 +486,16 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
   int bidx = 0x7fffffff;
   RowStats st;
   const int nvec = a.V / EPV;
-  for (int v0 = tid; v0 < nvec; v0 += kRowThreads * kBatch) {
+  const int per = (nvec + a.nsplit - 1) / a.nsplit;
+  const int vbeg = min(nvec, slice * per), vend = min(nvec, vbeg + per);
+  for (int v0 = vbeg + tid; v0 < vend; v0 += kRowThreads * kBatch) {
     // all of the round's loads first (raw vectors, or scalars already widened)
     uint4 raw[kVec ? kBatch : 1];
     float xs[kVec ? 1 : kBatch];
 #pragma unroll
     for (int j = 0; j < kBatch; ++j) {
       const int v = v0 + j * kRowThreads;
-      if (v < nvec) {
+      if (v < vend) {
         if constexpr (kVec) raw[j] = __ldcs(reinterpret_cast<const uint4*>(base) + v);
         else xs[j] = Act<T>::to_f(base[v]);
       }
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int v = v0 + j * kRowThreads;
-        if (v < nvec) {
+        if (v < vend) {
           const float m8 = Max8<T>::of(raw[j]);
           if (m8 > best || bidx == 0x7fffffff) {
             T tmp[EPV];
@@ -527,7 +530,7 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int v = v0 + j * kRowThreads;
-        if (v < nvec) {
+        if (v < vend) {
           T tmp[EPV];
           memcpy(tmp, &raw[j], 16);
 #pragma unroll
@@ -550,7 +553,7 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int v = v0 + j * kRowThreads;
-        if (v < nvec) {
+        if (v < vend) {
           if (xs[j] > best || bidx == 0x7fffffff) {  // indices rise within a thread: the first maximum stays
             best = xs[j];
             bidx = v;
@@ -563,7 +566,7 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const int v = v0 + j * kRowThreads;
-        if (v < nvec) st.add(xs[j] * t.k);
+        if (v < vend) st.add(xs[j] * t.k);
       }
     }
   }
@@ -588,15 +591,55 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
   }
   warp_best(v, ix);  // every warp merges; thread 0's results are used
   all.warp_merge();
+  if (a.nsplit > 1) {
+    // fold this slice into the row: the argmax through the row's key, the
+    // statistics through the slice's workspace entry; the row's last slice
+    // merges the entries in slice order (leaving key and counter at zero) and
+    // goes on as the row's CTA
+    if (tid == 0) {
+      atomicMax(&a.row_keys[row], argmax_key(v, ix));
+      t.split_stats[(size_t)row * a.nsplit + slice] = make_float4(all.m, all.z, all.s, 0.f);
+      __threadfence();  // the key and the entry are visible before the arrival is counted
+      const bool last = atomicAdd(&a.row_counters[row], 1u) == (unsigned)(a.nsplit - 1);
+      if (last) {
+        __threadfence();  // every slice's key update and entry are visible past this point
+        ix = (int)(0xffffffffu - (uint32_t)atomicExch(&a.row_keys[row], 0ull));
+        a.row_counters[row] = 0;
+        RowStats acc;
+        for (int q = 0; q < a.nsplit; ++q) {
+          const float4 o = __ldcg(t.split_stats + (size_t)row * a.nsplit + q);
+          RowStats ro;
+          ro.m = o.x;
+          ro.z = o.y;
+          ro.s = o.z;
+          acc.merge(ro);
+        }
+        all = acc;
+      }
+      s_slice_last = last;
+    }
+    __syncthreads();
+    if (!s_slice_last) return;
+  }
   finish_typical<T>(a, t, row, ix, all, sm, typ_ok);
 }
+
+inline int row_splits(int nrows, int nvec);
 
 template <typename T>
 cudaError_t launch_typical_t(const AcceptParams& a, const TypicalParams& t, cudaStream_t stream) {
   const int nrows = a.B * a.T;
+  AcceptParams p = a;
+  p.nsplit = 1;
   if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0)
-    return launch_pdl(typical_rows_kernel<T, false>, dim3(nrows), dim3(kRowThreads), 0, stream, a, t);
-  return launch_pdl(typical_rows_kernel<T, true>, dim3(nrows), dim3(kRowThreads), 0, stream, a, t);
+    return launch_pdl(typical_rows_kernel<T, false>, dim3(nrows), dim3(kRowThreads), 0, stream, p, t);
+  // split rows as the greedy kernel does, within the workspace's split entries
+  if (nrows <= kTypSplitRows) {
+    const int ns = row_splits(nrows, (int)(a.V / (16 / sizeof(T))));
+    p.nsplit = ns < kTypMaxSplits ? ns : kTypMaxSplits;
+  }
+  return launch_pdl(typical_rows_kernel<T, true>, dim3((unsigned)((long long)nrows * p.nsplit)), dim3(kRowThreads),
+                    0, stream, p, t);
 }
 
 // The fused kernel's commit stage: every row's CTA carries it, so it stays

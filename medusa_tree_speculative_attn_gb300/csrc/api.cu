@@ -298,7 +298,7 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
 // (rows split over several CTAs) each row's key [B*T] uint64 and slice
 // counter [B*T] uint32.
 struct AcceptWs {
-  size_t counters, argmax, stats, row_keys, row_counters, total;
+  size_t counters, argmax, stats, row_keys, row_counters, split_stats, total;
 };
 
 AcceptWs accept_ws(int batch, int tree_size) {
@@ -309,7 +309,9 @@ AcceptWs accept_ws(int batch, int tree_size) {
   w.stats = align_up(w.argmax + sizeof(int) * rows);
   w.row_keys = align_up(w.stats + sizeof(float4) * rows);
   w.row_counters = align_up(w.row_keys + sizeof(unsigned long long) * rows);
-  w.total = align_up(w.row_counters + sizeof(unsigned) * rows);
+  w.split_stats = align_up(w.row_counters + sizeof(unsigned) * rows);
+  const size_t split_rows = rows < (size_t)kTypSplitRows ? rows : (size_t)kTypSplitRows;
+  w.total = align_up(w.split_stats + sizeof(float4) * split_rows * kTypMaxSplits);
   return w;
 }
 
@@ -388,6 +390,7 @@ int mt_tree_accept_typical(int batch, int tree_size, int vocab, int max_depth,
   TypicalParams t{};
   t.k = k; t.epsilon = epsilon; t.delta = delta;
   t.stats = reinterpret_cast<float4*>(ws + w.stats);
+  t.split_stats = reinterpret_cast<float4*>(ws + w.split_stats);
   t.node_accept = node_accept;
   return cuda_status(launch_accept_typical(a, t, logits_dtype, stream));
 }

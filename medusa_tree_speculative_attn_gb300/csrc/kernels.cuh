@@ -95,7 +95,12 @@ struct TypicalParams {
   float epsilon, delta;    // threshold min(epsilon, delta * exp(-entropy))
   float4* stats;           // [B*T] per row (max of y, Z, threshold, unused), workspace
   int* node_accept;        // [B][T] each node's own test (1 at the root)
+  // rows split over AcceptParams::nsplit CTAs: each slice's (max of y, Z, S),
+  // [B*T][nsplit] (at most kTypSplitRows rows of kTypMaxSplits slices), workspace
+  float4* split_stats;
 };
+constexpr int kTypSplitRows = 1024;  // typical-acceptance rows are split only up to this many
+constexpr int kTypMaxSplits = 16;
 
 struct CommitParams {
   int B, T, Hkv, D, P, max_blocks, num_pages, max_depth, rel_width, elem_bytes;

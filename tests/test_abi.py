@@ -134,7 +134,7 @@ def test_fused_accept_commit_rejects_bad_arguments(lib):
 
 def test_typical_acceptance_rejects_bad_arguments(lib):
     P = ctypes.c_void_p
-    buf = (ctypes.c_char * 4096)()
+    buf = (ctypes.c_char * 16384)()
     p = ctypes.cast(buf, P)
     al = ctypes.c_void_p((ctypes.addressof(buf) + 255) // 256 * 256)
     f = lib.mt_tree_accept_typical
@@ -142,11 +142,11 @@ def test_typical_acceptance_rejects_bad_arguments(lib):
     ok = dict(temperature=1.0, epsilon=0.09, delta=0.3)
 
     def call(B=1, T=8, V=10, md=3, dt=0, t=ok["temperature"], e=ok["epsilon"], d=ok["delta"], ptrs=None,
-             ws=al, nbytes=2048):
+             ws=al, nbytes=8192):
         args = ptrs if ptrs is not None else [p] * 7
         return f(B, T, V, md, dt, args[0], args[1], args[2], t, e, d, args[3], args[4], args[5], args[6],
                  ws, nbytes, None)
-    assert lib.mt_tree_accept_workspace_size(1, 8) <= 2048
+    assert lib.mt_tree_accept_workspace_size(1, 8) <= 8192
     assert call(T=65) == -2 and call(V=0) == -1 and call(md=64) == -1 and call(dt=9) == -2
     assert call(B=0) == -1
     for bad in (dict(t=0.0), dict(t=-1.0), dict(t=float("nan")), dict(t=float("inf")), dict(t=1e-40),
@@ -164,7 +164,10 @@ def test_typical_acceptance_rejects_bad_arguments(lib):
 def test_accept_workspace_holds_typical_scratch(lib):
     lib.mt_tree_accept_workspace_size.restype = ctypes.c_size_t
     for B, T in ((1, 1), (16, 64), (3, 7)):
-        assert lib.mt_tree_accept_workspace_size(B, T) >= 256 + 4 * B + 20 * B * T
+        # status, counters, argmax and statistics per row, split-row keys and
+        # counters, and 16 split-row statistics entries per row (up to 1024 rows)
+        rows = B * T
+        assert lib.mt_tree_accept_workspace_size(B, T) >= 256 + 4 * B + 32 * rows + 256 * min(rows, 1024)
         assert lib.mt_tree_accept_workspace_size(B, T) % 256 == 0
 
 
