@@ -212,7 +212,9 @@ int mt_tree_attn_paged_noalloc(const mt_attn_desc* desc, const void* q, const vo
  *   tree_parents int32 [B][T]; every depth must be <= max_depth.
  *   workspace: mt_tree_accept_workspace_size(B, T) bytes, zero-filled before
  *   first use (status word, per-sequence arrival counters, which every call
- *   leaves at zero, and per-node scratch for typical acceptance). */
+ *   leaves at zero, per-node scratch for typical acceptance, and, for rows
+ *   split over several CTAs when the rows are few, a per-row key and counter,
+ *   also left at zero, and per-slice statistics). */
 size_t mt_tree_accept_workspace_size(int batch, int tree_size);
 int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
                           mt_dtype logits_dtype, const int32_t* tree_tokens,
