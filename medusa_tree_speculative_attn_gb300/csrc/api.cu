@@ -231,8 +231,9 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   sched.nrg = w.nrg; sched.G = w.G; sched.splits = d->num_splits;
   // fixed work of a piece in tile units: the tensor-core kernel streams a
   // tile in about 1 us and spends a few us on a piece's queries, epilogue
-  // and pipeline refill; the SIMT kernel's tiles are far slower
-  sched.seg_cost = kernel == MT_KERNEL_SIMT ? 1 : 4;
+  // and pipeline refill, more with two M tiles (measured best: 5 with two,
+  // 4 with one); the SIMT kernel's tiles are far slower
+  sched.seg_cost = kernel == MT_KERNEL_SIMT ? 1 : (w.rows_per_group > 128 && w.rows > 128 ? 5 : 4);
   sched.tile_pfx = pp.tile_pfx;
   pp.sched = sched;
   pp.piece_table = kernel == MT_KERNEL_SIMT ? nullptr : reinterpret_cast<int*>(ws + w.pieces);

@@ -81,50 +81,58 @@ struct Piece {
   int slot;                  // partial slot, or -1 for a direct write
 };
 
-__device__ __forceinline__ long long sched_total_tiles(const Sched& s) {
-  return (long long)s.tile_pfx[s.B] * s.Hkv * s.nrg;
+// The schedule's arithmetic is written over an index type I: 64-bit in the
+// attention kernels, and 32-bit in the prep kernel's table walk once it has
+// checked that the total cost times (G + 1) fits in 31 bits (every product
+// and quotient below is then the same in either type).
+template <typename I = long long>
+__device__ __forceinline__ I sched_total_tiles(const Sched& s) {
+  return (I)s.tile_pfx[s.B] * s.Hkv * s.nrg;
 }
 
 // Largest b with tile_pfx[b] * HR <= t (the sequence owning global tile t).
-__device__ __forceinline__ int sched_find_seq(const Sched& s, long long t) {
-  long long HR = (long long)s.Hkv * s.nrg;
+template <typename I>
+__device__ __forceinline__ int sched_find_seq(const Sched& s, I t) {
+  const I HR = (I)s.Hkv * s.nrg;
   int lo = 0, hi = s.B - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if ((long long)s.tile_pfx[mid] * HR <= t) lo = mid; else hi = mid - 1;
+    if ((I)s.tile_pfx[mid] * HR <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
 // Balanced mode: total cost, cost of a global tile, and the first global
 // tile at or past a cost (the total tile count W when there is none).
-__device__ __forceinline__ long long sched_total_cost(const Sched& s) {
-  return sched_total_tiles(s) + (long long)s.seg_cost * s.B * s.Hkv * s.nrg;
+template <typename I = long long>
+__device__ __forceinline__ I sched_total_cost(const Sched& s) {
+  return sched_total_tiles<I>(s) + (I)s.seg_cost * s.B * s.Hkv * s.nrg;
 }
 
 __device__ __forceinline__ long long sched_tile_cost(const Sched& s, long long t, long long seg) {
   return t + (long long)s.seg_cost * (seg + 1);
 }
 
-__device__ __forceinline__ long long sched_first_tile_at(const Sched& s, long long y) {
-  const long long HR = (long long)s.Hkv * s.nrg;
+template <typename I>
+__device__ __forceinline__ I sched_first_tile_at(const Sched& s, I y) {
+  const I HR = (I)s.Hkv * s.nrg;
   // sequence b's segments start at cost tile_pfx[b] * HR + seg_cost * HR * b
   int lo = 0, hi = s.B - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if ((long long)s.tile_pfx[mid] * HR + (long long)s.seg_cost * HR * mid <= y) lo = mid; else hi = mid - 1;
+    if ((I)s.tile_pfx[mid] * HR + (I)s.seg_cost * HR * mid <= y) lo = mid; else hi = mid - 1;
   }
   const int b = lo;
-  const long long base = (long long)s.tile_pfx[b] * HR + (long long)s.seg_cost * HR * b;
-  const long long nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
-  const long long per = nt + s.seg_cost;  // cost of one segment of sequence b
-  const long long off = y > base ? y - base : 0;
-  if (per == 0) return (long long)s.tile_pfx[b] * HR;
-  const long long k = off / per;
-  if (k >= HR) return (long long)s.tile_pfx[b + 1] * HR;
-  const long long r = off % per;
-  const long long j = r < s.seg_cost ? 0 : r - s.seg_cost;
-  return (long long)s.tile_pfx[b] * HR + k * nt + j;
+  const I base = (I)s.tile_pfx[b] * HR + (I)s.seg_cost * HR * b;
+  const I nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
+  const I per = nt + s.seg_cost;  // cost of one segment of sequence b
+  const I off = y > base ? y - base : 0;
+  if (per == 0) return (I)s.tile_pfx[b] * HR;
+  const I k = off / per;
+  if (k >= HR) return (I)s.tile_pfx[b + 1] * HR;
+  const I r = off % per;
+  const I j = r < s.seg_cost ? 0 : r - s.seg_cost;
+  return (I)s.tile_pfx[b] * HR + k * nt + j;
 }
 
 // CTA whose cost range holds cost x in balanced mode (X the total cost).
@@ -133,22 +141,23 @@ __device__ __forceinline__ int sched_cta_of(long long x, long long X, int G) {
 }
 
 // Iterator over the pieces of one CTA.
-struct PieceIter {
+template <typename I>
+struct PieceIterT {
   Sched s;
   int cta;
-  long long cur, end;  // balanced: global tile cursor; split mode: unit cursor
-  long long W;
+  I cur, end;  // balanced: global tile cursor; split mode: unit cursor
+  I W;
 
   __device__ void init(const Sched& sc, int c) {
     s = sc;
     cta = c;
     if (s.splits == 0) {
-      W = sched_total_tiles(s);
-      const long long X = sched_total_cost(s);
-      cur = sched_first_tile_at(s, X * c / s.G);
-      end = sched_first_tile_at(s, X * (c + 1) / s.G);
+      W = sched_total_tiles<I>(s);
+      const I X = sched_total_cost<I>(s);
+      cur = sched_first_tile_at<I>(s, X * c / s.G);
+      end = sched_first_tile_at<I>(s, X * (c + 1) / s.G);
     } else {
-      W = (long long)s.B * s.Hkv * s.nrg * s.splits;
+      W = (I)s.B * s.Hkv * s.nrg * s.splits;
       cur = W * c / s.G;
       end = W * (c + 1) / s.G;
     }
@@ -156,36 +165,36 @@ struct PieceIter {
 
   // Returns false when the CTA has no more work.
   __device__ bool next(Piece& p) {
-    long long HR = (long long)s.Hkv * s.nrg;
+    const I HR = (I)s.Hkv * s.nrg;
     while (cur < end) {
       if (s.splits == 0) {
-        int b = sched_find_seq(s, cur);
+        int b = sched_find_seq<I>(s, cur);
         int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
-        long long local = cur - (long long)s.tile_pfx[b] * HR;
+        I local = cur - (I)s.tile_pfx[b] * HR;
         int seg_in_b = (int)(local / nt);
         int j0 = (int)(local % nt);
-        long long seg_begin = cur - j0;
-        long long seg_end = seg_begin + nt;
-        long long stop = end < seg_end ? end : seg_end;
+        I seg_begin = cur - j0;
+        I seg_end = seg_begin + nt;
+        I stop = end < seg_end ? end : seg_end;
         p.b = b;
         p.kvh = seg_in_b / s.nrg;
         p.rg = seg_in_b % s.nrg;
-        p.seg = (int)((long long)b * HR + seg_in_b);
+        p.seg = (int)((I)b * HR + seg_in_b);
         p.tile_begin = j0;
         p.tile_end = j0 + (int)(stop - cur);
         p.slot = (j0 == 0 && stop == seg_end) ? -1 : p.seg + cta;
         cur = stop;
         return true;
       } else {
-        long long u = cur++;
+        I u = cur++;
         int k = (int)(u % s.splits);
         int seg = (int)(u / s.splits);
         int b = (int)(seg / HR);
         int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
-        int j0 = (int)((long long)nt * k / s.splits);
-        int j1 = (int)((long long)nt * (k + 1) / s.splits);
+        int j0 = (int)((I)nt * k / s.splits);
+        int j1 = (int)((I)nt * (k + 1) / s.splits);
         if (j0 >= j1) continue;
-        int seg_in_b = (int)(seg - (long long)b * HR);
+        int seg_in_b = (int)(seg - (I)b * HR);
         p.b = b;
         p.kvh = seg_in_b / s.nrg;
         p.rg = seg_in_b % s.nrg;
@@ -199,6 +208,7 @@ struct PieceIter {
     return false;
   }
 };
+using PieceIter = PieceIterT<long long>;
 
 // Arguments shared by both attention kernels and the combine kernel.
 struct AttnParams {

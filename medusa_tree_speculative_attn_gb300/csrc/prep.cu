@@ -152,8 +152,152 @@ __device__ void ancestor_masks(const PrepParams& a, int b, unsigned long long* s
   __syncwarp();
 }
 
+// Where one query or key/value row of the rotation loop goes: index() finds
+// the row's sequence and node, place() loads its prefix length and depth.
+struct RowPlace {
+  int b, i, L, depth;
+  bool live, is_q;
+
+  __device__ __forceinline__ void index(const PrepParams& a, long long grow, long long nq, long long nrows) {
+    live = grow < nrows;
+    if (!live) return;
+    is_q = grow < nq;
+    const long long row = is_q ? grow : grow - nq;
+    const int H = is_q ? a.Hq : a.Hkv;
+    if (row <= 0xffffffffLL && (long long)H * a.T <= 0xffffffffLL) {  // 32-bit division
+      const unsigned r32 = (unsigned)row, h = (unsigned)H;
+      i = (int)((r32 / h) % (unsigned)a.T);
+      b = (int)(r32 / (h * (unsigned)a.T));
+    } else {
+      i = (int)((row / H) % a.T);
+      b = (int)(row / ((long long)H * a.T));
+    }
+  }
+  __device__ __forceinline__ void place(const PrepParams& a) {
+    if (!live) return;
+    L = a.seq_lens[b];
+    depth = a.tree_depths[(size_t)b * a.T + i];
+  }
+};
+
+// Rotates one row as lane k of its lane group (the pairs (j, j + D/2) for j in
+// [8k, 8k + 8)) and stores it: a query into the workspace, a key (and its
+// value, unrotated) into its slot of the cache.
 template <typename T>
-__global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
+__device__ __forceinline__ void rotate_row(const PrepParams& a, const RowPlace& pl, long long grow, long long nq,
+                                           int k, int half) {
+  if (!pl.live) return;
+  const bool is_q = pl.is_q;
+  const long long row = is_q ? grow : grow - nq;
+  const int b = pl.b, i = pl.i, L = pl.L, depth = pl.depth;
+  const T* src = static_cast<const T*>(is_q ? a.q : a.k_new) + (size_t)row * a.D;
+  const typename Vec8<T>::type lo = Vec8<T>::load(src + 8 * k);
+  const typename Vec8<T>::type hi = Vec8<T>::load(src + half + 8 * k);
+  typename Vec8<T>::type vlo, vhi;
+  if (!is_q) {
+    const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
+    vlo = Vec8<T>::load(vn + 8 * k);
+    vhi = Vec8<T>::load(vn + half + 8 * k);
+  }
+  const long long pos = (long long)L + depth;
+  if (L < 0 || depth < 0 || pos >= a.max_pos) {
+    if (k == 0) set_status(a.status, L < 0 ? kStPages : kStTree);
+    return;
+  }
+  T* dst = nullptr;         // act-dtype destination of the rotated row
+  uint8_t* dst8 = nullptr;  // FP8 cache destination of a rotated key
+  if (is_q) {
+    dst = static_cast<T*>(a.q_rot) + (size_t)row * a.D;
+  } else {
+    const int kvh = (int)(row % a.Hkv);
+    const unsigned slot = (unsigned)L + (unsigned)i;  // L >= 0 and i < 64: no wrap
+    const unsigned pg = slot / (unsigned)a.P;
+    const int page = pg < (unsigned)a.max_blocks ? a.block_tables[(size_t)b * a.max_blocks + pg] : -1;
+    if (page < 0 || page >= a.num_pages) {
+      if (k == 0) set_status(a.status, kStPages);
+      return;
+    }
+    const size_t off = (((size_t)page * a.Hkv + kvh) * a.P + slot % (unsigned)a.P) * a.D;
+    if (a.cache_fp8) {
+      // FP8 cache: the codes of the raw value and (below) of the rotated key
+      dst8 = static_cast<uint8_t*>(a.k_cache) + off;
+      uint8_t* vc8 = static_cast<uint8_t*>(a.v_cache) + off;
+      store_e4m3x8<T>(vc8 + 8 * k, vlo, a.v_scale);
+      store_e4m3x8<T>(vc8 + half + 8 * k, vhi, a.v_scale);
+    } else {
+      dst = static_cast<T*>(a.k_cache) + off;
+      // raw value: this lane's two 8-element chunks
+      T* vc = static_cast<T*>(a.v_cache) + off;
+      Vec8<T>::store(vc + 8 * k, vlo);
+      Vec8<T>::store(vc + half + 8 * k, vhi);
+    }
+  }
+  const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * half + 8 * k);
+  T xl[8], xh[8], ol[8], oh[8];
+  memcpy(xl, &lo, sizeof(xl));
+  memcpy(xh, &hi, sizeof(xh));
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) {
+    const float4 c = cs[e / 2];  // (cos, sin) of pairs e and e + 1
+    float l0, h0, l1, h1;
+    rope_pair(Act<T>::to_f(xl[e]), Act<T>::to_f(xh[e]), c.x, c.y, l0, h0);
+    rope_pair(Act<T>::to_f(xl[e + 1]), Act<T>::to_f(xh[e + 1]), c.z, c.w, l1, h1);
+    ol[e] = Act<T>::from_f(l0);
+    ol[e + 1] = Act<T>::from_f(l1);
+    oh[e] = Act<T>::from_f(h0);
+    oh[e + 1] = Act<T>::from_f(h1);
+  }
+  typename Vec8<T>::type wl, wh;
+  memcpy(&wl, ol, sizeof(ol));
+  memcpy(&wh, oh, sizeof(oh));
+  if (dst8) {
+    store_e4m3x8<T>(dst8 + 8 * k, wl, a.k_scale);
+    store_e4m3x8<T>(dst8 + half + 8 * k, wh, a.k_scale);
+  } else {
+    Vec8<T>::store(dst + 8 * k, wl);
+    Vec8<T>::store(dst + half + 8 * k, wh);
+  }
+}
+
+// Whether every product and quotient of the piece walk fits in 32 bits: the
+// balanced schedule's total cost X (split mode: its unit count) times G + 1,
+// and split mode's tile counts times splits + 1.  total = tiles per segment,
+// summed over the sequences.
+__device__ __forceinline__ bool sched_fits_int(const Sched& s, int total) {
+  const long long HR = (long long)s.Hkv * s.nrg;
+  const long long lim = 1LL << 31;
+  if (s.splits == 0) return ((long long)total * HR + (long long)s.seg_cost * s.B * HR) * (s.G + 1) < lim;
+  return (long long)s.B * HR * s.splits * (s.G + 1) < lim && (long long)total * (s.splits + 1) < lim;
+}
+
+// Each CTA's piece list (one thread per CTA), with the index type I of the
+// schedule arithmetic.
+template <typename I>
+__device__ void walk_pieces(const PrepParams& a, const Sched& sc, const int* s_len) {
+  PieceRec* recs = reinterpret_cast<PieceRec*>(a.piece_table + sc.G);
+  for (int c = threadIdx.x; c < sc.G; c += blockDim.x) {
+    PieceIterT<I> it;
+    it.init(sc, c);
+    Piece p;
+    int n = 0;
+    while (it.next(p)) {
+      if (n == kMaxPieceRecs) {
+        n = -1;
+        break;
+      }
+      PieceRec r;
+      r.b = p.b; r.kvh = p.kvh; r.rg = p.rg; r.seg = p.seg;
+      r.tile_begin = p.tile_begin; r.tile_end = p.tile_end; r.slot = p.slot;
+      r.L = s_len[p.b];
+      recs[(size_t)c * kMaxPieceRecs + n] = r;
+      ++n;
+    }
+    a.piece_table[c] = n;
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPrepThreads, sizeof(T) == 4 ? 3 : 4) prep_kernel(PrepParams a) {
   const int tid = threadIdx.x;
   pdl_wait();
   if (blockIdx.x == 0) {
@@ -228,26 +372,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
       __syncthreads();
       Sched sc = a.sched;
       sc.tile_pfx = s_nt;
-      PieceRec* recs = reinterpret_cast<PieceRec*>(a.piece_table + sc.G);
-      for (int c = tid; c < sc.G; c += blockDim.x) {
-        PieceIter it;
-        it.init(sc, c);
-        Piece p;
-        int n = 0;
-        while (it.next(p)) {
-          if (n == kMaxPieceRecs) {
-            n = -1;
-            break;
-          }
-          PieceRec r;
-          r.b = p.b; r.kvh = p.kvh; r.rg = p.rg; r.seg = p.seg;
-          r.tile_begin = p.tile_begin; r.tile_end = p.tile_end; r.slot = p.slot;
-          r.L = s_len[p.b];
-          recs[(size_t)c * kMaxPieceRecs + n] = r;
-          ++n;
-        }
-        a.piece_table[c] = n;
-      }
+      if (sched_fits_int(sc, total)) walk_pieces<int>(a, sc, s_len);
+      else walk_pieces<long long>(a, sc, s_len);
     }
     return;
   }
@@ -261,91 +387,27 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(PrepParams a) {
   }
   // ---- rotations: B*T*Hq query rows, then B*T*Hkv key/value rows ----
   // A row is handled by D/16 lanes; lane k rotates the pairs (j, j + D/2) for
-  // j in [8k, 8k + 8) with 16-byte (8-element) loads and stores.  The row's
-  // own data is loaded before the prefix length and depth it is placed by.
+  // j in [8k, 8k + 8) with 16-byte (8-element) loads and stores.  The prefix
+  // length and depth that place a lane group's next row are loaded while the
+  // current row is rotated, so each trip waits on one round of loads.
   const int lanes_per_row = a.D / 16;
   const int rows_per_warp = 32 / lanes_per_row;
   const int lane = tid & 31;
   const int sub = lane / lanes_per_row, k = lane % lanes_per_row;
   const long long nq = (long long)a.B * a.T * a.Hq;
-  const long long nk = (long long)a.B * a.T * a.Hkv;
+  const long long nrows = nq + (long long)a.B * a.T * a.Hkv;
   const int half = a.D / 2;
-  for (long long row0 = gwarp * rows_per_warp; row0 < nq + nk; row0 += nwarps * rows_per_warp) {
-    long long row = row0 + sub;
-    if (row >= nq + nk) continue;
-    const bool is_q = row < nq;
-    if (!is_q) row -= nq;
-    const int H = is_q ? a.Hq : a.Hkv;
-    const int i = (int)((row / H) % a.T);
-    const int b = (int)(row / ((long long)H * a.T));
-    const T* src = static_cast<const T*>(is_q ? a.q : a.k_new) + (size_t)row * a.D;
-    const typename Vec8<T>::type lo_raw = Vec8<T>::load(src + 8 * k);
-    const typename Vec8<T>::type hi_raw = Vec8<T>::load(src + half + 8 * k);
-    typename Vec8<T>::type vlo, vhi;
-    if (!is_q) {
-      const T* vn = static_cast<const T*>(a.v_new) + (size_t)row * a.D;
-      vlo = Vec8<T>::load(vn + 8 * k);
-      vhi = Vec8<T>::load(vn + half + 8 * k);
-    }
-    const int L = a.seq_lens[b];
-    const int depth = a.tree_depths[(size_t)b * a.T + i];
-    const long long pos = (long long)L + depth;
-    if (L < 0 || depth < 0 || pos >= a.max_pos) {
-      if (k == 0) set_status(a.status, L < 0 ? kStPages : kStTree);
-      continue;
-    }
-    T* dst = nullptr;        // act-dtype destination of the rotated row
-    uint8_t* dst8 = nullptr;  // FP8 cache destination of a rotated key
-    if (is_q) {
-      dst = static_cast<T*>(a.q_rot) + (size_t)row * a.D;
-    } else {
-      const int kvh = (int)(row % a.Hkv);
-      const long long slot = (long long)L + i;
-      const int page = slot / a.P < a.max_blocks ? a.block_tables[(size_t)b * a.max_blocks + slot / a.P] : -1;
-      if (page < 0 || page >= a.num_pages) {
-        if (k == 0) set_status(a.status, kStPages);
-        continue;
-      }
-      const size_t off = (((size_t)page * a.Hkv + kvh) * a.P + slot % a.P) * a.D;
-      if (a.cache_fp8) {
-        // FP8 cache: the codes of the raw value and (below) of the rotated key
-        dst8 = static_cast<uint8_t*>(a.k_cache) + off;
-        uint8_t* vc8 = static_cast<uint8_t*>(a.v_cache) + off;
-        store_e4m3x8<T>(vc8 + 8 * k, vlo, a.v_scale);
-        store_e4m3x8<T>(vc8 + half + 8 * k, vhi, a.v_scale);
-      } else {
-        dst = static_cast<T*>(a.k_cache) + off;
-        // raw value: this lane's two 8-element chunks
-        T* vc = static_cast<T*>(a.v_cache) + off;
-        Vec8<T>::store(vc + 8 * k, vlo);
-        Vec8<T>::store(vc + half + 8 * k, vhi);
-      }
-    }
-    const float4* cs = reinterpret_cast<const float4*>(a.rope + (size_t)pos * half + 8 * k);
-    T lo[8], hi[8], olo[8], ohi[8];
-    memcpy(lo, &lo_raw, sizeof(lo));
-    memcpy(hi, &hi_raw, sizeof(hi));
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const float4 c = cs[e / 2];  // (cos, sin) of pairs e and e + 1
-      float l0, h0, l1, h1;
-      rope_pair(Act<T>::to_f(lo[e]), Act<T>::to_f(hi[e]), c.x, c.y, l0, h0);
-      rope_pair(Act<T>::to_f(lo[e + 1]), Act<T>::to_f(hi[e + 1]), c.z, c.w, l1, h1);
-      olo[e] = Act<T>::from_f(l0);
-      olo[e + 1] = Act<T>::from_f(l1);
-      ohi[e] = Act<T>::from_f(h0);
-      ohi[e + 1] = Act<T>::from_f(h1);
-    }
-    typename Vec8<T>::type wl, wh;
-    memcpy(&wl, olo, sizeof(olo));
-    memcpy(&wh, ohi, sizeof(ohi));
-    if (dst8) {
-      store_e4m3x8<T>(dst8 + 8 * k, wl, a.k_scale);
-      store_e4m3x8<T>(dst8 + half + 8 * k, wh, a.k_scale);
-    } else {
-      Vec8<T>::store(dst + 8 * k, wl);
-      Vec8<T>::store(dst + half + 8 * k, wh);
-    }
+  const long long stride = nwarps * rows_per_warp;
+  long long row0 = gwarp * rows_per_warp + sub;
+  RowPlace cur;
+  cur.index(a, row0, nq, nrows);
+  cur.place(a);
+  for (; row0 < nrows; row0 += stride) {
+    RowPlace nxt;
+    nxt.index(a, row0 + stride, nq, nrows);
+    nxt.place(a);
+    rotate_row<T>(a, cur, row0, nq, k, half);
+    cur = nxt;
   }
 }
 
