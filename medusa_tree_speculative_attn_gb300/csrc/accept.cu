@@ -63,6 +63,18 @@ __device__ __forceinline__ void warp_best(float& best, int& bidx) {
   }
 }
 
+// Counts one arrival at a counter in global memory and returns the count
+// before it.  The read-modify-write is acquire-release at GPU scope: the
+// caller's earlier writes (and atomics) become visible to whichever thread
+// later acquires through this counter, and the caller sees everything the
+// earlier arrivals released.  A CTA that finds itself last passes that view
+// on to its other threads through a block barrier.
+__device__ __forceinline__ unsigned count_arrival(unsigned* counter) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+  return old;
+}
+
 // Shared state of a sequence's path selection (one warp) and commit.
 struct FinishSmem {
   unsigned long long anc[kMaxTree];
@@ -226,13 +238,11 @@ __device__ void finish_row(const AcceptParams& a, const CommitParams& c, int row
   const int b = row / a.T;
   if (kCommit) commit_load_window(c, b, sm.seq_len, sm.commit);
   if (threadIdx.x == 0) {
-    a.argmax_out[row] = ix;
-    __threadfence();  // the argmax is visible before the arrival is
-    sm.last = atomicAdd(&a.counters[b], 1u) == (unsigned)(a.T - 1);
+    a.argmax_out[row] = ix;  // released by the arrival
+    sm.last = count_arrival(&a.counters[b]) == (unsigned)(a.T - 1);
   }
-  __syncthreads();
+  __syncthreads();  // the last CTA's threads see every row's argmax past this point
   if (!sm.last) return;
-  __threadfence();  // every other row's argmax is visible past this point
   if (threadIdx.x == 0) a.counters[b] = 0;  // left at zero for the next call
   if (threadIdx.x < 32) select_path(a, b, sm);
   if (kCommit) {
@@ -319,11 +329,10 @@ __global__ void __launch_bounds__(kRowThreads, 8) argmax_rows_kernel(AcceptParam
     // fold this slice into the row's key and count it; the row's last slice
     // takes the key (leaving it and the counter at zero) and goes on
     if (tid == 0) {
-      atomicMax(&a.row_keys[row], argmax_key(v, ix));
-      __threadfence();  // the key is updated before the arrival is counted
-      const bool last = atomicAdd(&a.row_counters[row], 1u) == (unsigned)(a.nsplit - 1);
+      atomicMax(&a.row_keys[row], argmax_key(v, ix));  // released by the arrival
+      const bool last = count_arrival(&a.row_counters[row]) == (unsigned)(a.nsplit - 1);
       if (last) {
-        __threadfence();  // every slice's key update is visible past this point
+        // every slice's key update is ordered before this exchange
         ix = (int)(0xffffffffu - (uint32_t)atomicExch(&a.row_keys[row], 0ull));
         a.row_counters[row] = 0;
       }
@@ -435,13 +444,11 @@ __device__ void finish_typical(const AcceptParams& a, const TypicalParams& t, in
     const float h = log2f(st.z) - st.s / st.z;  // entropy in bits
     const float thr = fminf(t.epsilon, t.delta * exp2f(-h));
     t.stats[row] = make_float4(st.m, st.z, thr, 0.f);
-    a.argmax_out[row] = ix;
-    __threadfence();  // the row's results are visible before the arrival is
-    sm.last = atomicAdd(&a.counters[b], 1u) == (unsigned)(a.T - 1);
+    a.argmax_out[row] = ix;  // both released by the arrival
+    sm.last = count_arrival(&a.counters[b]) == (unsigned)(a.T - 1);
   }
-  __syncthreads();
+  __syncthreads();  // the last CTA's threads see every row's results past this point
   if (!sm.last) return;
-  __threadfence();  // every other row's results are visible past this point
   if (threadIdx.x == 0) a.counters[b] = 0;
   if (threadIdx.x >= 32) return;
   const T* lg = static_cast<const T*>(a.logits);
@@ -599,10 +606,10 @@ __global__ void __launch_bounds__(kRowThreads, 8) typical_rows_kernel(AcceptPara
     if (tid == 0) {
       atomicMax(&a.row_keys[row], argmax_key(v, ix));
       t.split_stats[(size_t)row * a.nsplit + slice] = make_float4(all.m, all.z, all.s, 0.f);
-      __threadfence();  // the key and the entry are visible before the arrival is counted
-      const bool last = atomicAdd(&a.row_counters[row], 1u) == (unsigned)(a.nsplit - 1);
+      // the key update and the entry are released by the arrival
+      const bool last = count_arrival(&a.row_counters[row]) == (unsigned)(a.nsplit - 1);
       if (last) {
-        __threadfence();  // every slice's key update and entry are visible past this point
+        // every slice's key update and entry are ordered before what follows
         ix = (int)(0xffffffffu - (uint32_t)atomicExch(&a.row_keys[row], 0ull));
         a.row_counters[row] = 0;
         RowStats acc;

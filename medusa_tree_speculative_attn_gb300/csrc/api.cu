@@ -86,7 +86,7 @@ int layout_for(const mt_attn_desc* d, int kernel, WsLayout* w) {
   off = align_up(off + sizeof(int) * (size_t)(d->batch + 1));
   w->pieces = off;  // the tensor-core kernel's per-CTA piece lists
   if (kernel != MT_KERNEL_SIMT)
-    off = align_up(off + (sizeof(int) + sizeof(PieceRec) * kMaxPieceRecs) * (size_t)w->G);
+    off = align_up(off + sizeof(int) * (size_t)piece_rec_offset(w->G) + sizeof(PieceRec) * kMaxPieceRecs * (size_t)w->G);
   w->qrot = off;
   off = align_up(off + (size_t)elem_bytes(d->dtype) * d->batch * d->tree_size * d->num_q_heads *
                            d->head_dim);

@@ -253,12 +253,15 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8>::kThreads, 1)
   // table, queries, masks and block tables are read only past this wait
   pdl_wait();
   if (warp == C::kPvWarp) {
-    // this CTA's piece list (written by the prep kernel) into shared memory
+    // this CTA's piece list (written by the prep kernel) into shared memory:
+    // the first four records are loaded with the count, the rest (rare) after
+    const int* src = a.piece_table + piece_rec_offset(a.sched.G) + (size_t)blockIdx.x * kMaxPieceRecs * 8;
+    const int first = src[lane];
     const int n = a.piece_table[blockIdx.x];
-    if (lane == 0) *s_npieces = n;
-    const int* src = a.piece_table + a.sched.G + (size_t)blockIdx.x * kMaxPieceRecs * 8;
     int* dst = reinterpret_cast<int*>(s_pieces);
-    for (int e = lane; e < (n > 0 ? n : 0) * 8; e += 32) dst[e] = src[e];
+    dst[lane] = first;
+    if (lane == 0) *s_npieces = n;
+    for (int e = 32 + lane; e < (n > 0 ? n : 0) * 8; e += 32) dst[e] = src[e];
   }
   tc::tc_fence_before();
   __syncthreads();

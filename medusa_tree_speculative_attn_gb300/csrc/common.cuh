@@ -229,7 +229,7 @@ struct AttnParams {
   float4* part_o;                 // [slots][D/4][part_rows]: unnormalised O, 4 columns per entry
   float2* part_ml;                // [slots][part_rows] (max in log2 units, sum)
   Sched sched;
-  const int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs] (tensor-core kernel)
+  const int* piece_table;         // count[G], padded, + PieceRec[G][kMaxPieceRecs] (tensor-core kernel)
   unsigned long long wait_limit_ns;  // bound of every pipeline wait (tensor-core kernel)
   int test_stall;                    // tensor-core kernel: first wait on a barrier nothing completes
   int cache_fp8;                     // tensor-core kernel: the caches hold E4M3 codes of value / scale
@@ -239,13 +239,17 @@ struct AttnParams {
 // A CTA's pieces, listed ahead of time by the prep kernel (up to
 // kMaxPieceRecs; more is recorded as a count of -1), with the sequence's
 // prefix length, so that the attention kernel starts a piece without
-// dependent global loads.  Table layout: int count[G], then
-// PieceRec rec[G][kMaxPieceRecs].
+// dependent global loads.  Table layout: int count[G] (padded to a multiple
+// of 4), then PieceRec rec[G][kMaxPieceRecs], 16-byte aligned when the table
+// is.
 constexpr int kMaxPieceRecs = 32;
 
-struct PieceRec {
+struct __align__(16) PieceRec {
   int b, kvh, rg, seg, tile_begin, tile_end, slot, L;
 };
+
+// Offset of the records in the table, in ints.
+__host__ __device__ __forceinline__ int piece_rec_offset(int G) { return (G + 3) & ~3; }
 
 // Pieces from a shared-memory copy of the table, or from the schedule itself
 // when the table overflowed (n < 0).

@@ -52,7 +52,7 @@ struct PrepParams {
   unsigned long long* anc;  // [B][T]
   int* tile_pfx;            // [B + 1]
   Sched sched;              // the attention kernel's schedule (tile_pfx unused)
-  int* piece_table;         // count[G] + PieceRec[G][kMaxPieceRecs], or null
+  int* piece_table;         // count[G], padded, + PieceRec[G][kMaxPieceRecs], or null
   int cache_fp8;            // the caches hold FP8 E4M3 codes of value / scale
   float k_scale, v_scale;
 };

@@ -271,10 +271,10 @@ __device__ __forceinline__ bool sched_fits_int(const Sched& s, int total) {
 }
 
 // Each CTA's piece list (one thread per CTA), with the index type I of the
-// schedule arithmetic.
+// schedule arithmetic; a record is two 16-byte stores.
 template <typename I>
 __device__ void walk_pieces(const PrepParams& a, const Sched& sc, const int* s_len) {
-  PieceRec* recs = reinterpret_cast<PieceRec*>(a.piece_table + sc.G);
+  PieceRec* recs = reinterpret_cast<PieceRec*>(a.piece_table + piece_rec_offset(sc.G));
   for (int c = threadIdx.x; c < sc.G; c += blockDim.x) {
     PieceIterT<I> it;
     it.init(sc, c);
