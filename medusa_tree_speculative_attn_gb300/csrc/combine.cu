@@ -75,15 +75,18 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(Attn
   const long long W = s.splits == 0 ? sched_total_cost(s) : 0;  // balanced mode works in cost units
   // does partial slot slot0 + k of segment seg (nt tiles) hold a piece?
   auto piece_exists = [&](const ItemInfo& in, int k) -> bool {
-    if (in.all || k == 0 || k == in.count - 1) return true;
+    if (in.all) return true;
     if (s.splits == 0) {
       // the segment's tiles are one contiguous stretch of the cost axis: its
       // first and last owners hold tiles of it, and a CTA in between covers its
       // whole cost range inside it, so it holds tiles exactly when that range
       // is not empty
+      if (k == 0 || k == in.count - 1) return true;
       const int c = in.slot0 - in.seg + k;
       return W * (c + 1) / s.G > W * c / s.G;
     }
+    // split mode: key chunk k is [nt k / n, nt (k + 1) / n), empty (and never
+    // written) when the segment has fewer tiles than chunks
     return (long long)in.nt * k / s.splits < (long long)in.nt * (k + 1) / s.splits;
   };
   for (long long base = blockIdx.x; base < items; base += 32LL * gridDim.x) {

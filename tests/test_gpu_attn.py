@@ -70,6 +70,26 @@ def test_small_cases(dtype, case, splits):
             _check_scatter(w, step)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("splits", [3, 8])
+def test_split_chunks_past_short_segments_are_never_read(dtype, splits):
+    # with more key chunks than a segment has tiles, the leading chunks are
+    # empty and no kernel writes their partial slots: fill the workspace with
+    # NaN bytes (past the status word) so that reading one would show
+    kw = dict(B=3, Hq=4, Hkv=2, head_dim=128, prefix=("list", [16, 1, 70]),
+              tree=("fanout", (3, 2), 9), max_depth=2)
+    spec = workloads.custom("short_split", dtype=dtype, **kw)
+    for kernel in _kernels(dtype):
+        w = workloads.generate(spec, seed=3)
+        step = Step(w, kernel=kernel, num_splits=splits)
+        step.ws.fill_(0xFF)
+        step.ws[:256].zero_()
+        step.attn()
+        assert step.status()[0] == 0
+        assert torch.isfinite(step.out.float()).all()
+        _check_full(w, step)
+
+
 def test_tiny_tree_fp32():
     w = workloads.generate("tiny_tree_fp32", seed=0)
     step = Step(w)
