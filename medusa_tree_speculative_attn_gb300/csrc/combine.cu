@@ -30,6 +30,20 @@ __device__ __forceinline__ void merge(float& M, float& lsum, float4 (&acc)[PER],
   M = m_new;
 }
 
+// Four results rounded to the act dtype, stored as one 8-byte (16-bit types)
+// or 16-byte (fp32) shared-memory write.
+template <typename T>
+__device__ __forceinline__ void store4(T* p, float a, float b, float c, float d) {
+  if constexpr (sizeof(T) == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+  } else {
+    const T v[4] = {Act<T>::from_f(a), Act<T>::from_f(b), Act<T>::from_f(c), Act<T>::from_f(d)};
+    uint2 w;
+    memcpy(&w, v, 8);
+    *reinterpret_cast<uint2*>(p) = w;
+  }
+}
+
 constexpr int kWarps = 8;
 constexpr int kBlocksPerSm = 2;
 constexpr int kRound = 4;          // pieces whose loads are in flight together
@@ -165,13 +179,9 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(Attn
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        const int c = 4 * (warp + kWarps * e);
-        s_out[lane][c] = Act<T>::from_f(acc[e].x * inv);
-        s_out[lane][c + 1] = Act<T>::from_f(acc[e].y * inv);
-        s_out[lane][c + 2] = Act<T>::from_f(acc[e].z * inv);
-        s_out[lane][c + 3] = Act<T>::from_f(acc[e].w * inv);
-      }
+      for (int e = 0; e < PER; ++e)
+        store4<T>(&s_out[lane][4 * (warp + kWarps * e)], acc[e].x * inv, acc[e].y * inv, acc[e].z * inv,
+                  acc[e].w * inv);
       __syncthreads();
       // 32 rows x CH chunks, consecutive threads along a row
       for (int idx = tid; idx < 32 * CH; idx += blockDim.x) {
