@@ -147,10 +147,12 @@ struct PieceIterT {
   int cta;
   I cur, end;  // balanced: global tile cursor; split mode: unit cursor
   I W;
+  int bcur;    // balanced: the sequence owning cur, once found (-1 before)
 
   __device__ void init(const Sched& sc, int c) {
     s = sc;
     cta = c;
+    bcur = -1;
     if (s.splits == 0) {
       W = sched_total_tiles<I>(s);
       const I X = sched_total_cost<I>(s);
@@ -168,7 +170,12 @@ struct PieceIterT {
     const I HR = (I)s.Hkv * s.nrg;
     while (cur < end) {
       if (s.splits == 0) {
-        int b = sched_find_seq<I>(s, cur);
+        // the cursor only moves forward: after the first search, step to the
+        // largest sequence whose segments start at or before it
+        if (bcur < 0) bcur = sched_find_seq<I>(s, cur);
+        else
+          while (bcur + 1 < s.B && (I)s.tile_pfx[bcur + 1] * HR <= cur) ++bcur;
+        const int b = bcur;
         int nt = s.tile_pfx[b + 1] - s.tile_pfx[b];
         I local = cur - (I)s.tile_pfx[b] * HR;
         int seg_in_b = (int)(local / nt);
