@@ -169,11 +169,12 @@ def kernel_code_fingerprint() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str, kernel: str):
+def ncu_traffic(workload: str, kernel: str, cache: str = "act"):
     """DRAM bytes per launch of the tensor-core attention kernel from the
     committed ncu summary, or None when that capture does not describe the
-    kernel as it is now (different workload, kernel or code)."""
-    path = os.path.join(ROOT, "profiles", f"attn_tc_{workload}.md")
+    kernel as it is now (different workload, cache format, kernel or code)."""
+    name = f"attn_tc_e4m3_{workload}.md" if cache == "e4m3" else f"attn_tc_{workload}.md"
+    path = os.path.join(ROOT, "profiles", name)
     if kernel == "simt" or not os.path.exists(path):
         return None
     fields = {}
@@ -625,7 +626,7 @@ def run_ours(args, rank, world, local_rank):
         achieved = ab["attn"] / (main_avg * 1e-3) / 1e9
         roofline = {"kernel": "tree attention main kernel", "bound": "hbm", "achieved": achieved,
                     "peak": peak, "peak_source": peak_src, "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": ncu_traffic(args.workload, args.kernel), "ms_per_launch": main_avg,
+                    "traffic": ncu_traffic(args.workload, args.kernel, args.cache), "ms_per_launch": main_avg,
                     "alg_bytes_per_launch": ab["attn"]}
     # the whole tree_attn_paged call (prep, main kernel, combine) against the
     # same bytes

@@ -37,5 +37,9 @@ def test_traffic_only_for_the_captured_code(tmp_path, monkeypatch):
     assert bench.ncu_traffic("w", "auto") == 1234
     assert bench.ncu_traffic("w", "simt") is None      # another kernel
     assert bench.ncu_traffic("other", "auto") is None  # no capture for that workload
+    assert bench.ncu_traffic("w", "auto", "e4m3") is None  # a 16-bit capture for an FP8 cache
+    (tmp_path / "profiles" / "attn_tc_e4m3_w.md").write_text(
+        f"traffic_bytes_per_launch: 617\nkernel_code_sha256_16: {bench.kernel_code_fingerprint()}\n")
+    assert bench.ncu_traffic("w", "auto", "e4m3") == 617
     prof.write_text("traffic_bytes_per_launch: 1234\nkernel_code_sha256_16: 0000000000000000\n")
     assert bench.ncu_traffic("w", "auto") is None      # captured on other code
