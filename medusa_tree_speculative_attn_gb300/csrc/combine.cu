@@ -45,8 +45,6 @@ __device__ __forceinline__ void store4(T* p, float a, float b, float c, float d)
 }
 
 constexpr int kWarps = 8;
-constexpr int kBlocksPerSm = 2;
-constexpr int kRound = 4;          // pieces whose loads are in flight together
 constexpr int kPfxCached = 2048;  // tile prefixes copied to shared memory up to this batch
 
 // What a block needs to merge one item (segment, 32-row block).
@@ -62,11 +60,11 @@ struct ItemInfo {
 // in parallel instead of on every item's critical path), so that an item
 // whose segment was written directly costs nothing.  For an item, thread
 // (warp w, lane l) merges row l for the 4-column groups w, w + 8, ... (partial
-// reads coalesced along rows), kRound pieces per round with all their loads
+// reads coalesced along rows), ROUND pieces per round with all their loads
 // in flight; the block stages the merged rows in shared memory and writes them
-// out in 16-byte chunks along each row.
-template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(AttnParams a) {
+// out in 16-byte chunks along each row.  BLOCKS blocks are resident per SM.
+template <typename T, int D, int ROUND, int BLOCKS>
+__global__ void __launch_bounds__(kWarps * 32, BLOCKS) combine_kernel(AttnParams a) {
   constexpr int C4 = D / 4;                    // 4-column groups per row
   constexpr int PER = C4 / kWarps;             // groups per thread
   constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte output chunks per row
@@ -160,11 +158,11 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(Attn
           merge<PER>(M, lsum, acc, ml1, v1);
         }
       } else if (row_ok) {
-        for (int k = 0; k < in.count; k += kRound) {
-          float2 ml[kRound];
-          float4 v[kRound][PER];
+        for (int k = 0; k < in.count; k += ROUND) {
+          float2 ml[ROUND];
+          float4 v[ROUND][PER];
 #pragma unroll
-          for (int j = 0; j < kRound; ++j) {
+          for (int j = 0; j < ROUND; ++j) {
             ml[j] = make_float2(-INFINITY, 0.f);
             if (k + j < in.count && piece_exists(in, k + j)) {
               const size_t slot = (size_t)in.slot0 + k + j;
@@ -174,7 +172,7 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(Attn
             }
           }
 #pragma unroll
-          for (int j = 0; j < kRound; ++j) merge<PER>(M, lsum, acc, ml[j], v[j]);
+          for (int j = 0; j < ROUND; ++j) merge<PER>(M, lsum, acc, ml[j], v[j]);
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -198,13 +196,26 @@ __global__ void __launch_bounds__(kWarps * 32, kBlocksPerSm) combine_kernel(Attn
   }
 }
 
+template <typename T, int D, int ROUND, int BLOCKS>
+cudaError_t launch_v(const AttnParams& a, int sms, cudaStream_t stream) {
+  const long long items = (long long)a.B * a.Hkv * a.sched.nrg * ((a.part_rows + 31) / 32);
+  const long long grid = items < (long long)BLOCKS * sms ? items : (long long)BLOCKS * sms;
+  return launch_pdl(combine_kernel<T, D, ROUND, BLOCKS>, dim3((unsigned)(grid > 0 ? grid : 1)), dim3(kWarps * 32), 0,
+                    stream, a);
+}
+
+// A balanced schedule with at least a quarter as many segments as CTAs cuts a
+// segment into a few pieces (serving and 32k-token workloads: up to 3 and 4):
+// two pieces per round, at 3 blocks per SM, keep more items in flight.  Fewer
+// segments (batch 1: 32 segments over 152 CTAs, about 5 pieces each) or key
+// chunks take 4 pieces per round at 2 blocks per SM.
 template <typename T, int D>
 cudaError_t launch_t(const AttnParams& a, cudaStream_t stream) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const long long items = (long long)a.B * a.Hkv * a.sched.nrg * ((a.part_rows + 31) / 32);
-  const long long grid = items < (long long)kBlocksPerSm * sms ? items : (long long)kBlocksPerSm * sms;
-  return launch_pdl(combine_kernel<T, D>, dim3((unsigned)(grid > 0 ? grid : 1)), dim3(kWarps * 32), 0, stream, a);
+  const long long nseg = (long long)a.B * a.Hkv * a.sched.nrg;
+  if (a.sched.splits == 0 && 4 * nseg >= a.sched.G) return launch_v<T, D, 2, 3>(a, sms, stream);
+  return launch_v<T, D, 4, 2>(a, sms, stream);
 }
 
 }  // namespace
