@@ -651,13 +651,17 @@ cudaError_t launch_typical_t(const AcceptParams& a, const TypicalParams& t, cuda
 
 // The fused kernel's commit stage: every row's CTA carries it, so it stays
 // small enough for 7 CTAs per SM (the serving trees' five path entries of 8
-// bf16 heads of 128 fit in one pass).
+// bf16 heads of 128 fit in one pass).  A grid that fits 5 CTAs per SM in one
+// wave takes a stage twice that size, so that a sequence with more heads (32
+// heads of 128: 80 KB) moves in two passes instead of four.
 constexpr int kStageCap = 20 * 1024;
+constexpr int kStageCapWide = 40 * 1024;
+constexpr int kWideCtasPerSm = 5;
 
 // CTAs per row for the vector kernel: one, unless the rows are fewer than
 // about four CTAs per SM; then enough slices to reach that, each of at least
 // 256 vectors (two rounds of loads per thread).
-inline int row_splits(int nrows, int nvec) {
+inline int sm_count() {
   static std::atomic<int> sms_cached{0};
   int sms = sms_cached.load(std::memory_order_relaxed);
   if (sms <= 0) {
@@ -666,6 +670,11 @@ inline int row_splits(int nrows, int nvec) {
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     sms_cached.store(sms, std::memory_order_relaxed);
   }
+  return sms;
+}
+
+inline int row_splits(int nrows, int nvec) {
+  const int sms = sm_count();
   const long long target = 4LL * sms;
   if (nrows >= target) return 1;
   const int want = (int)((target + nrows - 1) / nrows);
@@ -673,18 +682,28 @@ inline int row_splits(int nrows, int nvec) {
   return most < 2 ? 1 : (want < most ? want : most);
 }
 
+// The commit's stage (16-byte entries) for a grid of nblocks CTAs.
+template <bool kCommit>
+int stage_vecs_for(const CommitParams& c, long long nblocks) {
+  if (!kCommit) return 0;
+  return commit_stage_vecs(c, nblocks <= (long long)kWideCtasPerSm * sm_count() ? kStageCapWide : kStageCap);
+}
+
 template <typename T, bool kCommit>
 cudaError_t launch_t(const AcceptParams& a, const CommitParams& c, cudaStream_t stream) {
   const int nrows = a.B * a.T;
-  const int sv = kCommit ? commit_stage_vecs(c, kStageCap) : 0;
-  const size_t smem = (size_t)sv * 16;
   AcceptParams p = a;
   p.nsplit = 1;
-  if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0)
-    return launch_pdl(argmax_scalar_kernel<T, kCommit>, dim3(nrows), dim3(kThreads), smem, stream, p, c, sv);
+  if (((long long)a.V * sizeof(T)) % 16 != 0 || (reinterpret_cast<uintptr_t>(a.logits) & 15) != 0) {
+    const int sv = stage_vecs_for<kCommit>(c, nrows);
+    return launch_pdl(argmax_scalar_kernel<T, kCommit>, dim3(nrows), dim3(kThreads), (size_t)sv * 16, stream, p,
+                      c, sv);
+  }
   p.nsplit = row_splits(nrows, (int)(a.V / (16 / sizeof(T))));
-  return launch_pdl(argmax_rows_kernel<T, kCommit>, dim3((unsigned)((long long)nrows * p.nsplit)),
-                    dim3(kRowThreads), smem, stream, p, c, sv);
+  const long long nblocks = (long long)nrows * p.nsplit;
+  const int sv = stage_vecs_for<kCommit>(c, nblocks);
+  return launch_pdl(argmax_rows_kernel<T, kCommit>, dim3((unsigned)nblocks), dim3(kRowThreads), (size_t)sv * 16,
+                    stream, p, c, sv);
 }
 
 template <bool kCommit>

@@ -206,15 +206,18 @@ cudaError_t launch_v(const AttnParams& a, int sms, cudaStream_t stream) {
 
 // A balanced schedule with at least a quarter as many segments as CTAs cuts a
 // segment into a few pieces (serving and 32k-token workloads: up to 3 and 4):
-// two pieces per round, at 3 blocks per SM, keep more items in flight.  Fewer
-// segments (batch 1: 32 segments over 152 CTAs, about 5 pieces each) or key
-// chunks take 4 pieces per round at 2 blocks per SM.
+// two pieces per round, at 3 blocks per SM, keep more items in flight.  With
+// no more items than SMs (batch 1: 64 items of about 5 pieces), every block
+// has an SM to itself and takes 8 pieces per round.  Otherwise (key chunks,
+// or many items of many pieces) 4 pieces per round at 2 blocks per SM.
 template <typename T, int D>
 cudaError_t launch_t(const AttnParams& a, cudaStream_t stream) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long nseg = (long long)a.B * a.Hkv * a.sched.nrg;
+  const long long items = nseg * ((a.part_rows + 31) / 32);
   if (a.sched.splits == 0 && 4 * nseg >= a.sched.G) return launch_v<T, D, 2, 3>(a, sms, stream);
+  if (items <= sms) return launch_v<T, D, 8, 1>(a, sms, stream);
   return launch_v<T, D, 4, 2>(a, sms, stream);
 }
 
