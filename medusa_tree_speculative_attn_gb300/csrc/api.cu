@@ -93,7 +93,7 @@ int layout_for(const mt_attn_desc* d, int kernel, WsLayout* w) {
   w->ml = off;
   off = align_up(off + sizeof(float2) * (size_t)nslots * w->part_rows);
   w->o = off;
-  off = align_up(off + sizeof(float) * (size_t)nslots * w->part_rows * d->head_dim);
+  off = align_up(off + (size_t)elem_bytes(d->dtype) * nslots * w->part_rows * d->head_dim);
   w->total = off;
   return MT_OK;
 }
@@ -251,7 +251,7 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
   ap.block_tables = block_tables; ap.seq_lens = seq_lens; ap.tree_depths = tree_depths;
   ap.out = out; ap.status = status;
   ap.anc = pp.anc;
-  ap.part_o = reinterpret_cast<float4*>(ws + w.o);
+  ap.part_o = ws + w.o;
   ap.part_ml = reinterpret_cast<float2*>(ws + w.ml);
   ap.sched = sched;
   ap.piece_table = pp.piece_table;

@@ -222,11 +222,15 @@ __global__ void __launch_bounds__(kThreads, kSimtCtasPerSm) attn_simt_kernel(Att
 #pragma unroll
         for (int c = 0; c < NC; ++c) dst[tx + 16 * c] = Act<T>::from_f(o[i][c] * inv);
       } else {
-        float* dst = reinterpret_cast<float*>(a.part_o);
+        // the partial output O / l in the act dtype, [slot][D/8][rows][8]
+        // (a row that saw no key of this piece has l = 0 and m = -inf: the
+        // combine skips it)
+        T* dst = static_cast<T*>(a.part_o);
+        const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
           const int col = tx + 16 * c;
-          dst[(((size_t)pc.slot * (D / 4) + col / 4) * a.part_rows + r) * 4 + col % 4] = o[i][c];
+          dst[(((size_t)pc.slot * (D / 8) + col / 8) * a.part_rows + r) * 8 + col % 8] = Act<T>::from_f(o[i][c] * inv);
         }
         if (tx == 0) a.part_ml[(size_t)pc.slot * a.part_rows + r] = make_float2(m[i], l[i]);
       }

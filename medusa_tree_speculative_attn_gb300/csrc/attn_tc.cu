@@ -578,7 +578,6 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8>::kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const unsigned long long tmask = a.T == 64 ? ~0ull : ((1ull << a.T) - 1ull);
     const float scale = a.scale_log2;
-    constexpr int C4 = D / 4;
     bool ok = true;
     auto wait_all = [&](uint64_t* bar, uint32_t parity) {
       bool rr = tc::mbar_wait(bar, parity, abort_flag, a.status, limit);
@@ -708,7 +707,8 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8>::kThreads, 1)
       if (!ok) break;
       tc::tc_fence_after();
       const int seg_row = m * 128 + r;
-      // an FP8 cache's V scale multiplies the output (direct) or the partial O
+      // the output, or the piece's partial output O / l (the combine weighs it by
+      // l), in the act dtype; an FP8 cache's V scale multiplies both
       const float vs = FP8 ? a.v_scale : 1.f;
       const float inv = (l_run > 0.f ? 1.f / l_run : 0.f) * vs;
 #pragma unroll 1
@@ -717,26 +717,28 @@ __global__ void __launch_bounds__(Cfg<D, MT, FP8>::kThreads, 1)
         tc::tmem_ld_x64(tmem + lane_addr + C::o_col(m) + 64 * hh, o);
         tc::tmem_ld_wait();
         if (row_ok) {
+          // 16-byte chunks of 8 columns: along the output row, or (a partial,
+          // [slot][D/8][rows]) chunk-major, so that consecutive rows (threads)
+          // write consecutive 16 B
+          uint4* dst;
+          size_t step;
           if (pc.slot < 0) {
             const int h = pc.kvh * a.g + row % a.g;
-            T* dst = static_cast<T*>(a.out) + (((size_t)pc.b * a.T + node) * a.Hq + h) * D + 64 * hh;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              T v[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] = Act<T>::from_f(__uint_as_float(o[8 * c + e]) * inv);
-              uint4 w;
-              memcpy(&w, v, 16);
-              reinterpret_cast<uint4*>(dst)[c] = w;
-            }
+            dst = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + (((size_t)pc.b * a.T + node) * a.Hq + h) * D +
+                                           64 * hh);
+            step = 1;
           } else {
-            // [slot][D/4][rows]: consecutive rows (threads) write consecutive 16 B
-            float4* dst = a.part_o + ((size_t)pc.slot * C4 + 16 * hh) * a.part_rows + seg_row;
+            dst = static_cast<uint4*>(a.part_o) + ((size_t)pc.slot * (D / 8) + 8 * hh) * a.part_rows + seg_row;
+            step = a.part_rows;
+          }
 #pragma unroll
-            for (int c = 0; c < 16; ++c)
-              dst[(size_t)c * a.part_rows] =
-                  make_float4(__uint_as_float(o[4 * c]) * vs, __uint_as_float(o[4 * c + 1]) * vs,
-                              __uint_as_float(o[4 * c + 2]) * vs, __uint_as_float(o[4 * c + 3]) * vs);
+          for (int c = 0; c < 8; ++c) {
+            T v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = Act<T>::from_f(__uint_as_float(o[8 * c + e]) * inv);
+            uint4 w;
+            memcpy(&w, v, 16);
+            dst[c * step] = w;
           }
         }
       }

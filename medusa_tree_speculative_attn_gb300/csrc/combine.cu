@@ -1,8 +1,9 @@
 // Split-KV combine: merges the partial softmax results of the pieces of one
 // segment (the Flash-Decoding style split that lmdeploy PR 1231 "[WIP] support
 // Medusa" plans for its tree-mask kernel).  For piece k with running maximum
-// m_k (base-2 units), sum l_k and unnormalised output O_k:
-//   M = max_k m_k,  w_k = 2^(m_k - M),  out = sum_k w_k O_k / sum_k w_k l_k,
+// m_k (base-2 units), sum l_k and output x_k = O_k / l_k (its own softmax
+// average, stored in the act dtype):
+//   M = max_k m_k,  w_k = 2^(m_k - M) l_k,  out = sum_k w_k x_k / sum_k w_k,
 // evaluated in one pass with a running maximum (pieces that saw no key of a
 // row, m_k = -inf, are skipped).
 // Segments covered by a single piece were written directly and are skipped.
@@ -12,36 +13,54 @@ namespace mt {
 
 namespace {
 
-// Fold one piece (max ml.x, sum ml.y, unnormalised columns v) into the running
+// One partial entry: 8 consecutive columns of one row in the act dtype, as
+// loaded (one 16-byte word, two for fp32).
+template <typename T>
+struct Chunk8 {
+  static constexpr int kWords = 8 * (int)sizeof(T) / 16;
+  uint4 w[kWords];
+  __device__ __forceinline__ void load(const T* p) {
+#pragma unroll
+    for (int k = 0; k < kWords; ++k) w[k] = reinterpret_cast<const uint4*>(p)[k];
+  }
+  __device__ __forceinline__ void to_f(float (&x)[8]) const {
+    T v[8];
+    memcpy(v, w, sizeof(v));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = Act<T>::to_f(v[e]);
+  }
+};
+
+// Fold one piece (max ml.x, sum ml.y, its output columns v) into the running
 // result; a piece that saw no key of the row (ml.x = -inf) is skipped.
-template <int PER>
-__device__ __forceinline__ void merge(float& M, float& lsum, float4 (&acc)[PER], float2 ml, const float4 (&v)[PER]) {
+template <typename T, int PER>
+__device__ __forceinline__ void merge(float& M, float& lsum, float (&acc)[PER][8], float2 ml,
+                                      const Chunk8<T> (&v)[PER]) {
   if (ml.x == -INFINITY) return;
   const float m_new = fmaxf(M, ml.x);
-  const float c_old = exp2f(M - m_new), c_new = exp2f(ml.x - m_new);
-  lsum = lsum * c_old + ml.y * c_new;
+  const float c_old = exp2f(M - m_new), c_new = exp2f(ml.x - m_new) * ml.y;
+  lsum = lsum * c_old + c_new;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
-    acc[e].x = acc[e].x * c_old + v[e].x * c_new;
-    acc[e].y = acc[e].y * c_old + v[e].y * c_new;
-    acc[e].z = acc[e].z * c_old + v[e].z * c_new;
-    acc[e].w = acc[e].w * c_old + v[e].w * c_new;
+    float x[8];
+    v[e].to_f(x);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[e][j] = acc[e][j] * c_old + x[j] * c_new;
   }
   M = m_new;
 }
 
-// Four results rounded to the act dtype, stored as one 8-byte (16-bit types)
-// or 16-byte (fp32) shared-memory write.
+// Eight results times inv, rounded to the act dtype, as one 16-byte (16-bit
+// types) or two (fp32) shared-memory writes.
 template <typename T>
-__device__ __forceinline__ void store4(T* p, float a, float b, float c, float d) {
-  if constexpr (sizeof(T) == 4) {
-    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
-  } else {
-    const T v[4] = {Act<T>::from_f(a), Act<T>::from_f(b), Act<T>::from_f(c), Act<T>::from_f(d)};
-    uint2 w;
-    memcpy(&w, v, 8);
-    *reinterpret_cast<uint2*>(p) = w;
-  }
+__device__ __forceinline__ void store8(T* p, const float (&x)[8], float inv) {
+  T v[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) v[e] = Act<T>::from_f(x[e] * inv);
+  uint4 w[8 * sizeof(T) / 16];
+  memcpy(w, v, sizeof(v));
+#pragma unroll
+  for (int k = 0; k < (int)(8 * sizeof(T) / 16); ++k) reinterpret_cast<uint4*>(p)[k] = w[k];
 }
 
 constexpr int kWarps = 8;
@@ -59,14 +78,14 @@ struct ItemInfo {
 // per item (which CTAs hold pieces of the segment: 64-bit schedule arithmetic
 // in parallel instead of on every item's critical path), so that an item
 // whose segment was written directly costs nothing.  For an item, thread
-// (warp w, lane l) merges row l for the 4-column groups w, w + 8, ... (partial
+// (warp w, lane l) merges row l for the 8-column entries w, w + 8, ... (partial
 // reads coalesced along rows), ROUND pieces per round with all their loads
 // in flight; the block stages the merged rows in shared memory and writes them
 // out in 16-byte chunks along each row.  BLOCKS blocks are resident per SM.
 template <typename T, int D, int ROUND, int BLOCKS>
 __global__ void __launch_bounds__(kWarps * 32, BLOCKS) combine_kernel(AttnParams a) {
-  constexpr int C4 = D / 4;                    // 4-column groups per row
-  constexpr int PER = C4 / kWarps;             // groups per thread
+  constexpr int C8 = D / 8;                    // 8-column partial entries per row
+  constexpr int PER = C8 / kWarps;             // entries per thread
   constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte output chunks per row
   __shared__ int s_pfx[kPfxCached + 1];
   __shared__ ItemInfo s_info[32];
@@ -135,9 +154,12 @@ __global__ void __launch_bounds__(kWarps * 32, BLOCKS) combine_kernel(AttnParams
       const int seg_in_b = in.seg % HR;
       const int b = in.seg / HR, kvh = seg_in_b / s.nrg, rg = seg_in_b % s.nrg;
       float M = -INFINITY, lsum = 0.f;
-      float4 acc[PER];
+      float acc[PER][8];
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int e = 0; e < PER; ++e)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[e][j] = 0.f;
+      const T* part = static_cast<const T*>(a.part_o);
       const int r = in.row0 + lane;
       const bool row_ok = r < PR && rg * RG + r < a.rows;
       if (row_ok && !in.all && s.splits == 0) {
@@ -151,16 +173,16 @@ __global__ void __launch_bounds__(kWarps * 32, BLOCKS) combine_kernel(AttnParams
           if (cta == prev) continue;
           prev = cta;
           const size_t slot = (size_t)in.seg + cta;
-          float4 v1[PER];
+          Chunk8<T> v1[PER];
           const float2 ml1 = a.part_ml[slot * PR + r];
 #pragma unroll
-          for (int e = 0; e < PER; ++e) v1[e] = a.part_o[(slot * C4 + warp + kWarps * e) * PR + r];
-          merge<PER>(M, lsum, acc, ml1, v1);
+          for (int e = 0; e < PER; ++e) v1[e].load(part + ((slot * C8 + warp + kWarps * e) * PR + r) * 8);
+          merge<T, PER>(M, lsum, acc, ml1, v1);
         }
       } else if (row_ok) {
         for (int k = 0; k < in.count; k += ROUND) {
           float2 ml[ROUND];
-          float4 v[ROUND][PER];
+          Chunk8<T> v[ROUND][PER];
 #pragma unroll
           for (int j = 0; j < ROUND; ++j) {
             ml[j] = make_float2(-INFINITY, 0.f);
@@ -168,18 +190,16 @@ __global__ void __launch_bounds__(kWarps * 32, BLOCKS) combine_kernel(AttnParams
               const size_t slot = (size_t)in.slot0 + k + j;
               ml[j] = a.part_ml[slot * PR + r];
 #pragma unroll
-              for (int e = 0; e < PER; ++e) v[j][e] = a.part_o[(slot * C4 + warp + kWarps * e) * PR + r];
+              for (int e = 0; e < PER; ++e) v[j][e].load(part + ((slot * C8 + warp + kWarps * e) * PR + r) * 8);
             }
           }
 #pragma unroll
-          for (int j = 0; j < ROUND; ++j) merge<PER>(M, lsum, acc, ml[j], v[j]);
+          for (int j = 0; j < ROUND; ++j) merge<T, PER>(M, lsum, acc, ml[j], v[j]);
         }
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
 #pragma unroll
-      for (int e = 0; e < PER; ++e)
-        store4<T>(&s_out[lane][4 * (warp + kWarps * e)], acc[e].x * inv, acc[e].y * inv, acc[e].z * inv,
-                  acc[e].w * inv);
+      for (int e = 0; e < PER; ++e) store8<T>(&s_out[lane][8 * (warp + kWarps * e)], acc[e], inv);
       __syncthreads();
       // 32 rows x CH chunks, consecutive threads along a row
       for (int idx = tid; idx < 32 * CH; idx += blockDim.x) {

@@ -233,7 +233,7 @@ struct AttnParams {
   void* out;
   int* status;
   const unsigned long long* anc;  // [B][T]
-  float4* part_o;                 // [slots][D/4][part_rows]: unnormalised O, 4 columns per entry
+  void* part_o;                   // [slots][D/8][part_rows] entries of 8 act values: O / l of the piece
   float2* part_ml;                // [slots][part_rows] (max in log2 units, sum)
   Sched sched;
   const int* piece_table;         // count[G], padded, + PieceRec[G][kMaxPieceRecs] (tensor-core kernel)
