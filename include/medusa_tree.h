@@ -151,7 +151,9 @@ int mt_rope_destroy(mt_rope* rope);
  * attention, node i's rotated key and raw value are written to logical slot
  * L_b + i (the scratch region), where mt_kv_commit later finds them; slots
  * below L_b are never written.  Accumulation in fp32, output rounded to nearest
- * even in the act dtype.
+ * even in the act dtype.  Where the schedule splits a (sequence, KV head) into
+ * pieces, each piece's own softmax output is rounded to the act dtype first
+ * and the fp32 merge is rounded again (the same tolerance holds).
  *   q      [B][T][Hq][D]    act   (not rotated)
  *   k_new  [B][T][Hkv][D]   act   (the tree tokens' keys, not rotated)
  *   v_new  [B][T][Hkv][D]   act
