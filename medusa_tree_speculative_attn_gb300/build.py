@@ -68,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     newest = max(os.path.getmtime(o) for o in objs)
     if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
         tmp = LIB + ".tmp"
-        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["--cudart", "static"]
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["--cudart", "static", "-ldl"]
         subprocess.run(cmd, check=True, capture_output=not verbose)
         os.replace(tmp, LIB)
     return LIB

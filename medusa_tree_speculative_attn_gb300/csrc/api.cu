@@ -5,8 +5,19 @@
 #include <cstring>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/medusa_tree.h"
 #include "kernels.cuh"
+
+// One NVTX range per library call, named after its C entry point, for a
+// timeline tool (nothing is recorded unless such a tool is attached).
+struct mt_call_range {
+  explicit mt_call_range(const char* name) { nvtxRangePushA(name); }
+  ~mt_call_range() { nvtxRangePop(); }
+  mt_call_range(const mt_call_range&) = delete;
+  mt_call_range& operator=(const mt_call_range&) = delete;
+};
 
 // Bound of the tensor-core kernel's pipeline waits, and the timeout test hook
 // (mt_debug_set_wait); read by every attention call.
@@ -196,6 +207,7 @@ int mt_tree_attn_paged(const mt_attn_desc* d, const void* q, const void* k_new, 
                        const int32_t* seq_lens, const int32_t* tree_parents,
                        const int32_t* tree_depths, const mt_rope* rope, void* out,
                        void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  const mt_call_range range("mt_tree_attn_paged");
   int st = check_desc(d);
   if (st != MT_OK) return st;
   if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_tables || !seq_lens ||
@@ -334,6 +346,7 @@ int mt_tree_accept_greedy(int batch, int tree_size, int vocab, int max_depth,
                           int32_t* argmax_out, int32_t* accept_len, int32_t* accept_path,
                           int32_t* next_token, void* workspace, size_t ws_bytes,
                           cudaStream_t stream) {
+  const mt_call_range range("mt_tree_accept_greedy");
   if (batch < 1 || batch > (1 << 24) / kMaxTree) return MT_ERR_INVALID_ARG;
   if (tree_size < 1 || tree_size > kMaxTree) return MT_ERR_UNSUPPORTED;
   if (vocab < 1 || max_depth < 0 || max_depth >= kMaxTree) return MT_ERR_INVALID_ARG;
@@ -363,6 +376,7 @@ int mt_tree_accept_typical(int batch, int tree_size, int vocab, int max_depth,
                            float temperature, float epsilon, float delta, int32_t* node_accept,
                            int32_t* accept_len, int32_t* accept_path, int32_t* next_token,
                            void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  const mt_call_range range("mt_tree_accept_typical");
   if (batch < 1 || batch > (1 << 24) / kMaxTree) return MT_ERR_INVALID_ARG;
   if (tree_size < 1 || tree_size > kMaxTree) return MT_ERR_UNSUPPORTED;
   if (vocab < 1 || max_depth < 0 || max_depth >= kMaxTree) return MT_ERR_INVALID_ARG;
@@ -400,6 +414,7 @@ int mt_kv_commit(const mt_attn_desc* d, int max_depth, const int32_t* accept_pat
                  const int32_t* accept_len, void* k_cache, void* v_cache, int32_t* block_tables,
                  int32_t* seq_lens, int32_t* released_pages, void* status_ws,
                  cudaStream_t stream) {
+  const mt_call_range range("mt_kv_commit");
   int st = check_desc(d);
   if (st != MT_OK) return st;
   if (max_depth < 0 || max_depth >= kMaxTree) return MT_ERR_INVALID_ARG;
@@ -427,6 +442,7 @@ int mt_tree_accept_commit(const mt_attn_desc* d, int vocab, int max_depth, mt_dt
                           int32_t* accept_path, int32_t* next_token, void* k_cache, void* v_cache,
                           int32_t* block_tables, int32_t* seq_lens, int32_t* released_pages,
                           void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  const mt_call_range range("mt_tree_accept_commit");
   int st = check_desc(d);
   if (st != MT_OK) return st;
   const int batch = d->batch, tree_size = d->tree_size;
@@ -467,6 +483,7 @@ int mt_tree_candidates(int batch, int tree_size, int heads, int vocab, mt_dtype 
                        const void* root_logits, const void* head_logits,
                        const int32_t* tree_parents, int32_t* tree_tokens, void* status_ws,
                        cudaStream_t stream) {
+  const mt_call_range range("mt_tree_candidates");
   if (batch < 1 || batch > kMaxBatch || heads < 1 || heads >= kMaxTree || vocab < 1)
     return MT_ERR_INVALID_ARG;
   if (tree_size < 1 || tree_size > kMaxTree) return MT_ERR_UNSUPPORTED;
