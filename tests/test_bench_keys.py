@@ -1,6 +1,7 @@
-"""Host-side logic of bench.py that decides whether a committed ncu capture
-still describes the attention kernel: the fingerprint of its code ignores
-comments and blank lines and changes with any code edit."""
+"""Host-side logic of bench.py: whether a committed ncu capture still
+describes the attention kernel (the fingerprint of its code ignores comments
+and blank lines and changes with any code edit), the algorithmic bytes the
+roofline lines divide by, and the whole-job rate."""
 import os
 import shutil
 
@@ -43,3 +44,24 @@ def test_traffic_only_for_the_captured_code(tmp_path, monkeypatch):
     assert bench.ncu_traffic("w", "auto", "e4m3") == 617
     prof.write_text("traffic_bytes_per_launch: 1234\nkernel_code_sha256_16: 0000000000000000\n")
     assert bench.ncu_traffic("w", "auto") is None      # captured on other code
+
+
+def test_algorithmic_bytes_of_the_profiled_workload():
+    # the serving workload as bench.py draws it (seed 1, rank 0): the bytes the
+    # roofline lines divide by, as the committed profiles state them
+    import workloads
+    w = workloads.generate("serve_b16_gqa_bf16", seed=bench.rank_seed(1, 0), with_logits=False)
+    ab = bench.algorithmic_bytes(w)
+    assert ab["attn"] == 314_421_248
+    B, T, Hq, Hkv, D = w["B"], w["T"], w["Hq"], w["Hkv"], w["head_dim"]
+    assert ab["tree_qo"] == B * T * Hq * D * 2 * 2       # bf16 q in, out written
+    assert ab["attn"] == ab["prefix_kv"] + ab["tree_qo"] + ab["tree_kv"]
+    # an FP8 cache halves the cached bytes only
+    ab8 = bench.algorithmic_bytes(w, 1)
+    assert ab8["attn"] == 165_599_232
+    assert ab8["prefix_kv"] * 2 == ab["prefix_kv"] and ab8["tree_qo"] == ab["tree_qo"]
+
+
+def test_whole_job_rate_counts_every_rank():
+    assert bench.whole_job_rate(1024, 1, 0.125) == 1024 / 0.125e-3
+    assert bench.whole_job_rate(1024, 4, 0.125) == 4 * 1024 / 0.125e-3
